@@ -1,0 +1,89 @@
+"""Seeded synthetic inputs shared by the CUDA path's tests, the bench and the oracle checks.
+
+This module holds no attention arithmetic: it only draws q, k, v. Both sides of every
+parity test consume the same bf16 buffers made here.
+
+Recipe: a CPU ``torch.Generator`` seeded with the workload's seed draws q, then k, then
+v with ``randn`` in fp32 (shape [B, H, T, d]); each is multiplied by ``std`` and cast to
+bf16 with round-to-nearest-even. For the "spiky" workload one key row per (b, h),
+at an index drawn afterwards from the same generator uniformly in [128, T), is
+multiplied by 8 in fp32 before the cast, so that every query that sees that key meets
+a large jump of the running row max in the middle of its scan. The pages' workloads
+use random bf16 q/k/v at GPT-2 124M head shapes (12 heads of width 64) and a length
+sweep up to 16k ("Hand-written FlashAttention", steps ④ and ⑤).
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    T: int
+    d: int
+    causal: bool
+    seed: int
+    std: float = 1.0
+    spike: str | None = None   # None, "k" or "q": which tensor gets one ×8 row per head
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def with_causal(self, causal: bool) -> "Workload":
+        return Workload(self.name, self.B, self.H, self.T, self.d, causal, self.seed,
+                        self.std, self.spike)
+
+
+SWEEP_T = (512, 1024, 2048, 4096, 8192, 16384)
+
+WORKLOADS = {
+    "tiny_causal": Workload("tiny_causal", 1, 2, 256, 64, True, 0),
+    "ragged_t1000": Workload("ragged_t1000", 2, 12, 1000, 64, True, 1),
+    "gpt2_layer_spiky": Workload("gpt2_layer_spiky", 4, 12, 1024, 64, True, 2, 0.5, "k"),
+    "gpt2_layer_spiky_q": Workload("gpt2_layer_spiky_q", 4, 12, 1024, 64, True, 2, 0.5, "q"),
+    "wide_head_t16k": Workload("wide_head_t16k", 2, 16, 16384, 128, True, 10),
+}
+for _i, _t in enumerate(SWEEP_T):
+    WORKLOADS[f"sweep_t{_t}"] = Workload(f"sweep_t{_t}", 4, 12, _t, 64, True, 3 + _i)
+
+
+def make_qkv(B: int, H: int, T: int, d: int, seed: int, std: float = 1.0,
+             spike: str | None = None):
+    """Draw (q, k, v) as contiguous bf16 CPU tensors of shape [B, H, T, d]."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    shape = (B, H, T, d)
+    q = torch.randn(shape, generator=g, dtype=torch.float32)
+    k = torch.randn(shape, generator=g, dtype=torch.float32)
+    v = torch.randn(shape, generator=g, dtype=torch.float32)
+    if std != 1.0:
+        q.mul_(std)
+        k.mul_(std)
+        v.mul_(std)
+    if spike is not None:
+        if T <= 128:
+            raise ValueError("a spiky workload needs T > 128")
+        rows = torch.randint(128, T, (B, H), generator=g)
+        target = {"k": k, "q": q}[spike]
+        for b in range(B):
+            for h in range(H):
+                target[b, h, int(rows[b, h])] *= 8.0
+    return (q.to(torch.bfloat16).contiguous(), k.to(torch.bfloat16).contiguous(),
+            v.to(torch.bfloat16).contiguous())
+
+
+def workload_qkv(w: Workload):
+    return make_qkv(w.B, w.H, w.T, w.d, w.seed, w.std, w.spike)
+
+
+def to_f64_numpy(t: torch.Tensor):
+    """Exact bf16 → fp64 numpy view for the oracle (bf16 values are exact in fp64)."""
+    return t.detach().to("cpu", torch.float64).numpy()

@@ -1,0 +1,23 @@
+"""CPU oracle for the exact attention forward pass.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports, links or runs this
+package: only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` use it. It shares no code with the CUDA path, and it imports nothing
+from the product package.
+
+Pages cited in this package (by title and section):
+
+* [HW-FA]  "手写 FlashAttention:拆开 SDPA 这个黑盒" (Hand-written FlashAttention),
+           learn-llm.fim.ai chapter 19, steps ①–⑤.
+* [KCS]    "内核案例研究：Flash Attention", the cnblogs translation of
+           "Kernel case study: Flash Attention" (towardsdatascience).
+"""
+
+from .naive import (  # noqa: F401
+    attention,
+    attention_rows,
+    online_softmax_trace,
+    online_weighted_sum,
+    safe_softmax,
+    scores,
+)

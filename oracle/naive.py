@@ -1,0 +1,184 @@
+"""Plain, slow fp64 oracle for scaled-dot-product attention (forward only).
+
+TEST INFRASTRUCTURE ONLY: never imported by the product path.
+
+What is computed, per (batch b, head h), for query rows i and key rows j of one
+sequence of length T (the naive form that [HW-FA] step ① writes out as
+S = QKᵀ/√d → softmax → P·V, and [KCS] "注意力算法" draws):
+
+    S[i, j]  = scale · q_i · k_j                      (scale = 1/√d in every workload)
+    S[i, j]  = −∞           where causal and j > i    ([HW-FA] step ③: the upper-right
+                                                       part of the score grid is masked)
+    m_i      = max_j S[i, j]                          (safe softmax: [HW-FA] step ②
+                                                       "why subtract the max",
+                                                       [KCS] "指数中的数值稳定性")
+    P[i, j]  = exp(S[i, j] − m_i) / Σ_j exp(S[i, j] − m_i)
+    O_i      = Σ_j P[i, j] · v_j
+    LSE_i    = m_i + ln Σ_j exp(S[i, j] − m_i)        (the per-row logsumexp that
+                                                       [HW-FA] step ④ says the forward
+                                                       keeps for the backward pass;
+                                                       natural log of the scaled scores)
+
+Inputs are upcast exactly to fp64 (bf16 → fp64 is exact) and every step runs in fp64
+with numpy; matrix products use numpy's BLAS. Nothing is tiled and there is no online
+recurrence here: the whole score row of a query is materialised. Rows are processed
+in chunks only to bound memory, and each row's result depends on that row alone, so
+chunking changes no arithmetic.
+
+The scalar online recurrence of [HW-FA] step ② (running max m, running sum l rescaled
+by exp(m_old − m_new), accumulator rescaled by the same factor, one final ÷l) is given
+separately by :func:`online_softmax_trace` and :func:`online_weighted_sum`, so that the
+tests can pin the recurrence itself against the one-pass definition.
+
+Pinned by ``tests/test_oracle.py`` (closed forms, invariants, brute force and
+planted-mistake checks); nothing here is "parity unpinned".
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# Rows of S materialised at once; a chunk of 512 rows at T = 16384 is 64 MB of fp64.
+_ROW_CHUNK = 512
+
+
+def _as_f64(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------------------
+# Steps of the definition. Each is a separate function so that the tests can plant a
+# mistake in exactly one step and check that some pin catches it.
+# --------------------------------------------------------------------------------------
+
+def scores(q_rows: np.ndarray, k: np.ndarray, scale: float) -> np.ndarray:
+    """S = scale · Q Kᵀ for the given query rows ([HW-FA] step ①). Shapes [R,d],[T,d] → [R,T]."""
+    return scale * (q_rows @ k.T)
+
+
+def apply_causal_mask(s: np.ndarray, rows: np.ndarray) -> np.ndarray:
+    """Set S[r, j] = −∞ where key j lies after query row rows[r] ([HW-FA] step ③).
+
+    Key j is visible to query i iff j ≤ i. Query and key sequences have the same
+    length here, so top-left and bottom-right alignment of the mask coincide.
+    """
+    T = s.shape[1]
+    j = np.arange(T)[None, :]
+    return np.where(j > rows[:, None], -np.inf, s)
+
+
+def safe_softmax(s: np.ndarray) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Row-wise softmax with the row max subtracted first ([HW-FA] step ②; [KCS] safe softmax).
+
+    Returns (P, m, l): the probabilities, the row max m and the row sum
+    l = Σ_j exp(S[i,j] − m_i). Every exponent is ≤ 0, so nothing overflows.
+    """
+    m = np.max(s, axis=1, keepdims=True)
+    e = np.exp(s - m)
+    l = np.sum(e, axis=1, keepdims=True)
+    return e / l, m[:, 0], l[:, 0]
+
+
+def weighted_values(p: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """O = P · V ([HW-FA] step ①, the last product of the naive form)."""
+    return p @ v
+
+
+def logsumexp_from(m: np.ndarray, l: np.ndarray) -> np.ndarray:
+    """LSE_i = m_i + ln l_i, natural log of Σ_j exp(S[i,j]) ([HW-FA] step ④ on the backward pass)."""
+    return m + np.log(l)
+
+
+# --------------------------------------------------------------------------------------
+# Public entry points.
+# --------------------------------------------------------------------------------------
+
+def attention_rows(q, k, v, causal: bool, scale: float, rows) -> tuple[np.ndarray, np.ndarray]:
+    """O and LSE for selected query rows of ONE (batch, head).
+
+    q, k, v: [T, d] arrays (any real dtype; upcast to fp64). rows: 1-D int array of
+    query indices in [0, T). Returns (O [R, d] fp64, LSE [R] fp64).
+    """
+    q = _as_f64(q)
+    k = _as_f64(k)
+    v = _as_f64(v)
+    rows = np.asarray(rows, dtype=np.int64)
+    s = scores(q[rows], k, scale)
+    if causal:
+        s = apply_causal_mask(s, rows)
+    p, m, l = safe_softmax(s)
+    return weighted_values(p, v), logsumexp_from(m, l)
+
+
+def attention(q, k, v, causal: bool, scale: float) -> tuple[np.ndarray, np.ndarray]:
+    """Exact attention forward for all heads.
+
+    q, k, v: [B, H, T, d] arrays. Returns (O [B,H,T,d] fp64, LSE [B,H,T] fp64).
+    """
+    q = _as_f64(q)
+    k = _as_f64(k)
+    v = _as_f64(v)
+    B, H, T, d = q.shape
+    o = np.empty((B, H, T, d), dtype=np.float64)
+    lse = np.empty((B, H, T), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            for r0 in range(0, T, _ROW_CHUNK):
+                rows = np.arange(r0, min(T, r0 + _ROW_CHUNK))
+                o[b, h, rows], lse[b, h, rows] = attention_rows(
+                    q[b, h], k[b, h], v[b, h], causal, scale, rows)
+    return o, lse
+
+
+# --------------------------------------------------------------------------------------
+# The online recurrence, as [HW-FA] step ② states it, for pinning the recurrence.
+# --------------------------------------------------------------------------------------
+
+def online_softmax_trace(x, block: int):
+    """Read the scores ``x`` ``block`` at a time, keeping only m and l ([HW-FA] step ②).
+
+    m is the largest score read so far and l = Σ exp(x − m) over the scores read so
+    far, taken relative to the current m. When a block raises the max, the old l is
+    multiplied by alpha = exp(m_old − m_new) before the block's own terms are added.
+
+    Returns a list with one tuple per block: (scores read, m, l, alpha). At the first
+    block alpha is exp(−∞) = 0. softmax(x) = exp(x − m_last) / l_last.
+    """
+    x = [float(t) for t in x]
+    m = -math.inf
+    l = 0.0
+    trace = []
+    for start in range(0, len(x), block):
+        xb = x[start:start + block]
+        m_new = max(m, max(xb))
+        alpha = math.exp(m - m_new) if m != -math.inf else 0.0
+        l = l * alpha + sum(math.exp(t - m_new) for t in xb)
+        m = m_new
+        trace.append((start + len(xb), m, l, alpha))
+    return trace
+
+
+def online_weighted_sum(x, vals, block: int):
+    """softmax(x) · vals by the blocked recurrence of [HW-FA] step ②.
+
+    acc holds Σ exp(x − m)·v relative to the m current when each term was added;
+    when the max rises, acc and l are both multiplied by the same
+    alpha = exp(m_old − m_new); after the last block the result is acc / l (the
+    division done once, at the end). ``vals`` is [n, d].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    vals = np.asarray(vals, dtype=np.float64)
+    m = -np.inf
+    l = 0.0
+    acc = np.zeros(vals.shape[1], dtype=np.float64)
+    for start in range(0, x.shape[0], block):
+        xb = x[start:start + block]
+        m_new = max(m, float(xb.max()))
+        alpha = math.exp(m - m_new) if m != -np.inf else 0.0
+        p = np.exp(xb - m_new)
+        l = l * alpha + float(p.sum())
+        acc = acc * alpha + p @ vals[start:start + block]
+        m = m_new
+    return acc / l, m, l

@@ -1,0 +1,137 @@
+"""CPU tests of the oracle against its pins, plus planted-mistake checks showing the
+pins would catch a plausible error in any one step of the oracle."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.naive as oa
+from tests import oracle_pins as pins
+
+
+@pytest.mark.parametrize("pin", pins.ORACLE_PINS + pins.RECURRENCE_PINS,
+                         ids=lambda p: p.__name__)
+def test_oracle_pin(pin):
+    pin(oa)
+
+
+def test_page_facts_are_consistent():
+    """The numbers the pages print agree with the mathematics they describe."""
+    f = pins.load_page_facts()
+    assert math.exp(f["fp16_exp_overflow_arg"]) > f["fp16_max"] > math.exp(f["fp16_exp_overflow_arg"] - 1)
+    fp32_max = float(np.finfo(np.float32).max)
+    assert math.exp(f["fp32_exp_overflow_near"] - 1) < fp32_max < math.exp(f["fp32_exp_overflow_near"])
+    assert abs(math.exp(88) - f["kcs_e88"]) / f["kcs_e88"] < 0.01
+    assert abs(2.0 ** 127 - f["kcs_2pow127"]) / f["kcs_2pow127"] < 0.01
+    assert abs(math.log2(math.e) - f["log2e"]) < 5e-5
+
+
+def test_oracle_package_exports():
+    for name in ("attention", "attention_rows", "online_softmax_trace", "online_weighted_sum"):
+        assert callable(getattr(oracle, name))
+
+
+# --------------------------------------------------------------------------- planted mistakes
+
+def _no_scale(q_rows, k, scale):
+    return q_rows @ k.T
+
+
+def _mask_wrong_way(s, rows):
+    j = np.arange(s.shape[1])[None, :]
+    return np.where(j < rows[:, None], -np.inf, s)
+
+
+def _mask_drops_diagonal(s, rows):
+    j = np.arange(s.shape[1])[None, :]
+    return np.where(j >= rows[:, None], -np.inf, s)
+
+
+def _no_mask(s, rows):
+    return s
+
+
+def _softmax_no_max(s):
+    e = np.exp(s)
+    l = e.sum(axis=1, keepdims=True)
+    return e / l, np.zeros(s.shape[0]), l[:, 0]
+
+
+def _softmax_unnormalised(s):
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    return e, m[:, 0], e.sum(axis=1)
+
+
+def _softmax_wrong_axis(s):
+    m = s.max(axis=0, keepdims=True)
+    e = np.exp(s - m)
+    l = e.sum(axis=0, keepdims=True)
+    return e / l, s.max(axis=1), np.exp(s - s.max(axis=1, keepdims=True)).sum(axis=1)
+
+
+def _values_transposed(p, v):
+    return p.T @ v
+
+
+def _lse_base2(m, l):
+    return m + np.log2(l)
+
+
+def _lse_without_max(m, l):
+    return np.log(l)
+
+
+def _trace_no_rescale(x, block):
+    m, l, out = -math.inf, 0.0, []
+    for s in range(0, len(x), block):
+        xb = list(x[s:s + block])
+        m = max(m, max(xb))
+        l = l + sum(math.exp(t - m) for t in xb)
+        out.append((s + len(xb), m, l, 1.0))
+    return out
+
+
+def _weighted_no_acc_rescale(x, vals, block):
+    x = np.asarray(x, float)
+    vals = np.asarray(vals, float)
+    m, l, acc = -np.inf, 0.0, np.zeros(vals.shape[1])
+    for s in range(0, len(x), block):
+        xb = x[s:s + block]
+        m_new = max(m, xb.max())
+        a = 0.0 if m == -np.inf else math.exp(m - m_new)
+        p = np.exp(xb - m_new)
+        l = l * a + p.sum()
+        acc = acc + p @ vals[s:s + block]
+        m = m_new
+    return acc / l, m, l
+
+
+MUTANTS = {
+    "scores:no_scale": ("scores", _no_scale),
+    "mask:wrong_direction": ("apply_causal_mask", _mask_wrong_way),
+    "mask:drops_diagonal": ("apply_causal_mask", _mask_drops_diagonal),
+    "mask:none": ("apply_causal_mask", _no_mask),
+    "softmax:no_max_subtraction": ("safe_softmax", _softmax_no_max),
+    "softmax:unnormalised": ("safe_softmax", _softmax_unnormalised),
+    "softmax:wrong_axis": ("safe_softmax", _softmax_wrong_axis),
+    "values:transposed": ("weighted_values", _values_transposed),
+    "lse:base2": ("logsumexp_from", _lse_base2),
+    "lse:without_max": ("logsumexp_from", _lse_without_max),
+    "trace:no_rescale": ("online_softmax_trace", _trace_no_rescale),
+    "weighted:no_acc_rescale": ("online_weighted_sum", _weighted_no_acc_rescale),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, monkeypatch):
+    attr, broken = MUTANTS[name]
+    monkeypatch.setattr(oa, attr, broken)
+    failed = pins.run_all(oa, pins.ORACLE_PINS + pins.RECURRENCE_PINS)
+    assert failed, f"no pin caught the planted mistake {name}"
+
+
+def test_unmodified_oracle_passes_every_pin():
+    assert pins.run_all(oa, pins.ORACLE_PINS + pins.RECURRENCE_PINS) == []
