@@ -1,0 +1,386 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact attention forward on GB300.
+
+Workload (one "step"): causal attention forward, bf16, B=4, H=12, d=64, one launch at each
+T in {512, 1024, 2048, 4096, 8192, 16384} (the length sweep at GPT-2 124M head shapes).
+The headline `value` is the sweep's total algorithmic FLOPs (causal = half of 4·B·H·T²·d)
+divided by the device time of the launches, in TFLOP/s, with the inputs already resident
+in HBM. `per_T` breaks it down. `e2e` is the same metric through the public API with the
+inputs in pinned host memory and the host<->device copies inside the timed region.
+
+L2: each step touches ~0.8 GB of distinct inputs and outputs (more than 6× the 129 MB L2),
+so every launch reads inputs last touched a full step earlier.
+
+`--impl reference` times the fp64 CPU oracle (the plain definition, numpy) on this machine's
+host cores on a bounded sample of the same workload and prints the same JSON line.
+
+Launch: `python bench.py [--gpus N --steps K --warmup W]`; for N > 1 under
+`torch.distributed.run`, each rank runs an independent replica of the workload on its own
+GPU (the forward needs no exchange between GPUs), the slowest rank's time is taken and
+`value` sums the work of all ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+B, H, D = 4, 12, 64
+SWEEP = (512, 1024, 2048, 4096, 8192, 16384)
+METRIC = "attn fwd TFLOP/s (bf16, B4 H12 d64, T 512\u201316k, causal) and % of tensor peak"
+WORKLOAD = "causal attention forward, bf16, B4 H12 d64, T sweep 512-16384 (one launch per T per step)"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return (float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), float(p["hbm_gbs"]),
+                "measured")
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, pw = [], [], []
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        # "under load": samples within 30% of the highest clock seen or drawing > 40% of max power
+        pmax = max(pw) if pw else 0.0
+        load = [s for s, p in zip(sm, pw) if p > 0.4 * pmax] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(mx), "samples": len(sm),
+                "power_w_max": pmax, "reasons": sorted(reasons)}
+
+
+def _smi_index(cuda_index: int) -> str:
+    """nvidia-smi names GPUs by physical index or UUID; map through CUDA_VISIBLE_DEVICES."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+    if vis:
+        parts = [x.strip() for x in vis.split(",") if x.strip()]
+        if cuda_index < len(parts):
+            return parts[cuda_index]
+    return str(cuda_index)
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- CPU oracle arm
+
+def _oracle_sample(budget_s: float):
+    """Time the fp64 oracle on sampled causal query rows at every T of the sweep; returns
+    (algorithmic FLOPs done, seconds, description). Rows are sampled evenly over the
+    sequence, so causal row lengths average T/2 like the full workload."""
+    import numpy as np
+
+    import oracle
+    from exact_attention_23_gb300 import inputs
+    rows_per_T = 128
+    work = []
+    for i, T in enumerate(SWEEP):
+        q, k, v = inputs.make_qkv(1, 1, T, D, seed=3 + i)
+        rows = np.linspace(0, T - 1, rows_per_T).astype(np.int64)
+        work.append((T, inputs.to_f64_numpy(q[0, 0]), inputs.to_f64_numpy(k[0, 0]),
+                     inputs.to_f64_numpy(v[0, 0]), rows))
+    flops = 0.0
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        for T, q, k, v, rows in work:
+            oracle.attention_rows(q, k, v, True, D ** -0.5, rows)
+            flops += float(np.sum(4.0 * (rows + 1) * D))
+        passes += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    desc = (f"{rows_per_T} query rows per T (evenly spaced, causal) of one head at each T in "
+            f"{list(SWEEP)}, d=64, repeated {passes}x; FLOPs counted as 4·(i+1)·d per row i")
+    return flops, dt, desc
+
+
+def _cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    per_step = max(0.5, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        _oracle_sample(per_step)
+    fl, dt = 0.0, 0.0
+    desc = ""
+    for _ in range(args.steps):
+        f, t, desc = _oracle_sample(per_step)
+        fl += f
+        dt += t
+    value = fl / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC,
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "d": D, "T": list(SWEEP), "causal": True,
+                   "parallelism": "cpu oracle (host cores)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+
+    import exact_attention_23_gb300 as fa
+    from exact_attention_23_gb300 import inputs
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    sweep = [args.T] if args.T else list(SWEEP)
+    sets = []
+    for i, T in enumerate(sweep):
+        q, k, v = inputs.make_qkv(B, H, T, D, seed=3 + SWEEP.index(T) if T in SWEEP else 100 + T)
+        qd, kd, vd = (t.to(dev) for t in (q, k, v))
+        o = torch.empty_like(qd)
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+        sets.append((T, q, k, v, qd, kd, vd, o, lse))
+    flops_step = sum(fa.flops(B, H, T, D, True) for T in sweep)
+    scale = D ** -0.5
+
+    def launch(s):
+        T, _, _, _, qd, kd, vd, o, lse = s
+        rc = fa.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                       B, H, T, D, 1, scale, stream.cuda_stream)
+        if rc != fa.FA_OK:
+            raise fa.FAError(rc, "fa_fwd")
+
+    for _ in range(args.warmup):
+        for s in sets:
+            launch(s)
+    torch.cuda.synchronize(dev)
+
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in sets] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(_smi_index(dev.index))
+    sampler.start()
+    time.sleep(0.3)
+    _barrier(ws)
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for it in range(args.steps):
+        for j, s in enumerate(sets):
+            ev[it][j][0].record(stream)
+            launch(s)
+            ev[it][j][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    _barrier(ws)
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = _max_over_ranks(elapsed_ms, ws)
+    launches = args.steps * len(sets)
+
+    bf16_peak, bf16_sus, hbm_peak, peak_kind = _peaks()
+    per_T = []
+    for j, s in enumerate(sets):
+        T = s[0]
+        ms = statistics.mean(ev[it][j][0].elapsed_time(ev[it][j][1]) for it in range(args.steps))
+        fl = fa.flops(B, H, T, D, True)
+        by = fa.hbm_bytes(B, H, T, D)
+        per_T.append({"T": T, "ms": ms, "tflops": fl / ms / 1e9,
+                      "frac_of_sustained": fl / ms / 1e9 / bf16_sus,
+                      "gbs": by / ms / 1e6, "frac_hbm": by / ms / 1e6 / hbm_peak})
+    dom = max(per_T, key=lambda r: fa.flops(B, H, r["T"], D, True))
+    value = ws * flops_step * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # ---- end to end: pinned host inputs -> device -> forward -> host, per step
+    e2e_steps = max(1, min(args.steps, 10))
+    pinned = []
+    h2d = d2h = 0
+    for (T, q, k, v, qd, kd, vd, o, lse) in sets:
+        hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        pinned.append((hq, hk, hv, ho, hl))
+        h2d += 3 * q.numel() * 2
+        d2h += o.numel() * 2 + lse.numel() * 4
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    _barrier(ws)
+    torch.cuda.synchronize(dev)
+    e_start.record(stream)
+    for _ in range(e2e_steps):
+        for s, (hq, hk, hv, ho, hl) in zip(sets, pinned):
+            T, _, _, _, qd, kd, vd, o, lse = s
+            qd.copy_(hq, non_blocking=True)
+            kd.copy_(hk, non_blocking=True)
+            vd.copy_(hv, non_blocking=True)
+            fa.fwd(qd, kd, vd, causal=True, out=o, lse=lse)
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = _max_over_ranks(e_start.elapsed_time(e_end), ws)
+    e2e_value = ws * flops_step * e2e_steps / (e_ms * 1e-3) / 1e12
+
+    result = None
+    if rank == 0:
+        cpu = None
+        if ws == 1 and not args.no_cpu_baseline:
+            fl, dt, desc = _oracle_sample(args.cpu_seconds)
+            cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+                   "sample": desc + "; numpy/BLAS default threads"}
+        result = {
+            "metric": METRIC,
+            "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 q/k/v)",
+            "config": {"workload": WORKLOAD if not args.T else f"causal attention forward, bf16, B4 H12 d64, T={args.T}",
+                       "B": B, "H": H, "d": D, "T": sweep, "causal": True,
+                       "parallelism": f"replicas{ws}" if ws > 1 else "single GPU",
+                       "l2": "inputs larger than L2: ~0.8 GB of distinct tensors per step" if not args.T else "single T"},
+            "frac_of_peak": {"sustained": value / ws / bf16_sus, "burst": value / ws / bf16_peak,
+                             "peak_kind": peak_kind},
+            "per_T": per_T,
+            "roofline": {"bound": "tensor", "achieved": dom["tflops"], "peak": bf16_sus,
+                         "unit": "TFLOP/s", "frac": dom["tflops"] / bf16_sus,
+                         "traffic": args.traffic,
+                         "kernel": f"fa_fwd_kernel<64,causal> at T={dom['T']} "
+                                   f"({fa.flops(B, H, dom['T'], D, True):.4g} FLOP per launch; "
+                                   f"peak = {peak_kind} sustained bf16)"},
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(result), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--T", type=int, default=0, help="time one length instead of the sweep")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

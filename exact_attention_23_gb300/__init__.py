@@ -1,0 +1,91 @@
+"""Exact attention forward for GB300 (sm_103a).
+
+``fwd(q, k, v, causal)`` returns ``(o, lse)`` for contiguous bf16 CUDA tensors of shape
+[B, H, T, d] (d = 64 or 128): o = softmax(scale·QKᵀ [+causal mask])·V in bf16 and the
+per-row natural-log logsumexp in fp32. The work is done by the CUDA kernels of
+``libfa.so`` through its C ABI (include/fa.h); this module only allocates the outputs
+with PyTorch and passes pointers and the current stream.
+"""
+
+from __future__ import annotations
+
+import math
+
+from ._binding import (  # noqa: F401
+    EXPORTS,
+    FA_ERR_INVALID_ARG,
+    FA_ERR_LAUNCH,
+    FA_ERR_MISALIGNED,
+    FA_ERR_TIMEOUT,
+    FA_ERR_UNSUPPORTED_DEVICE,
+    FA_FLAG_TEST_STARVE_Q,
+    FA_OK,
+    FAError,
+    fa_fwd,
+    fa_fwd_ex,
+    lib,
+    strerror,
+    version,
+)
+
+
+def _check(t, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be bfloat16")
+    if t.dim() != 4 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous [B, H, T, d] tensor")
+
+
+def fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=None,
+        status=None, timeout_ns: int = 0, flags: int = 0):
+    """Attention forward through libfa.so on the current CUDA stream.
+
+    Returns (o, lse). ``out``/``lse`` may be given to reuse buffers. ``status``, an
+    optional int32 CUDA tensor of one element, receives FA_ERR_TIMEOUT if an internal
+    wait of the kernel ever gives up.
+    """
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    if q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k and v must have the same shape")
+    B, H, T, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out")
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    st_ptr = None if status is None else status.data_ptr()
+    with torch.cuda.device(q.device):
+        rc = fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                       lse.data_ptr(), B, H, T, d, causal, scale, st_ptr, timeout_ns, flags,
+                       stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd")
+    return out, lse
+
+
+def flops(B: int, H: int, T: int, d: int, causal: bool) -> float:
+    """Algorithmic FLOPs of one forward: 4·B·H·T²·d (two T×T×d products), halved when
+    causal (the convention the throughput figures are quoted in)."""
+    f = 4.0 * B * H * T * T * d
+    return f / 2.0 if causal else f
+
+
+def hbm_bytes(B: int, H: int, T: int, d: int) -> float:
+    """Algorithmic HBM bytes of one forward: read q, k, v once, write o (bf16) and lse (fp32)."""
+    return B * H * T * (4.0 * d * 2 + 4.0)
+
+
+def q_tiles(T: int, rows: int = 128) -> int:
+    """Query-row tiles of ``rows`` rows covering a sequence of length T."""
+    return -(-T // rows)

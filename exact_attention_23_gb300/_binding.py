@@ -1,0 +1,77 @@
+"""ctypes binding of libfa.so (include/fa.h), with the same names as the C ABI.
+
+Argument marshalling only: every step of the attention computation runs in the CUDA
+kernels of libfa.so. PyTorch is used to own device memory and to name the stream.
+There is no fallback: if the library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_MISALIGNED = 2
+FA_ERR_UNSUPPORTED_DEVICE = 3
+FA_ERR_LAUNCH = 4
+FA_ERR_TIMEOUT = 5
+FA_FLAG_TEST_STARVE_Q = 1
+
+# Every symbol include/fa.h declares.
+EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_strerror", "fa_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({strerror(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfa.so (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with exact_attention_23_gb300.build.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+            L.fa_fwd.restype = i
+            L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp,
+                                    ctypes.c_ulonglong, ctypes.c_uint, vp]
+            L.fa_fwd_ex.restype = i
+            L.fa_strerror.argtypes = [i]
+            L.fa_strerror.restype = ctypes.c_char_p
+            L.fa_version.argtypes = []
+            L.fa_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().fa_strerror(int(status)).decode()
+
+
+def version() -> str:
+    return lib().fa_version().decode()
+
+
+def fa_fwd(q, k, v, o, lse, B, H, T, d, causal, scale, stream) -> int:
+    """Raw call: integer addresses in, status out."""
+    return lib().fa_fwd(q, k, v, o, lse, B, H, T, d, int(bool(causal)), float(scale), stream)
+
+
+def fa_fwd_ex(q, k, v, o, lse, B, H, T, d, causal, scale, status, timeout_ns, flags,
+              stream) -> int:
+    return lib().fa_fwd_ex(q, k, v, o, lse, B, H, T, d, int(bool(causal)), float(scale),
+                           status, int(timeout_ns), int(flags), stream)

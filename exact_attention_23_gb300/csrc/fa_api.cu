@@ -1,0 +1,163 @@
+// Host side of the C ABI declared in include/fa.h: argument validation, tensor-map
+// encoding for the TMA loads, and the launch on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_launch.h"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (no link-time
+// dependency on libcuda).
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+constexpr int kMaxDevices = 64;
+// 0 = unknown, 1 = supported (cc 10.3), 2 = unsupported
+int g_dev_state[kMaxDevices];
+std::mutex g_dev_mu;
+
+int check_device(int* dev_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return FA_ERR_UNSUPPORTED_DEVICE;
+  }
+  *dev_out = dev;
+  if (dev >= kMaxDevices) return FA_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_dev_state[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_UNSUPPORTED_DEVICE;
+    }
+    g_dev_state[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return g_dev_state[dev] == 1 ? FA_OK : FA_ERR_UNSUPPORTED_DEVICE;
+}
+
+// 3-D map over a [B·H][T][d] bf16 tensor: dim 0 = d (contiguous), dim 1 = T, dim 2 = B·H.
+// Boxes are 64 columns (128 bytes, the 128-byte swizzle span) × 128 rows × 1 head. Rows
+// past T read as zeros, so a ragged last tile never touches the next head.
+bool encode_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, int T, int d, int BH) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(T),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(T) * static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_version(void) { return "fa-gb300 0.1.0 sm_103a"; }
+
+const char* fa_strerror(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case FA_ERR_UNSUPPORTED_DEVICE: return "no CUDA device of compute capability 10.3 (sm_103a)";
+    case FA_ERR_LAUNCH: return "kernel launch failed";
+    case FA_ERR_TIMEOUT: return "an internal wait of the kernel timed out";
+    default: return "unknown status";
+  }
+}
+
+int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int T, int d, int causal, float scale, int* status, unsigned long long timeout_ns,
+              unsigned int flags, void* stream) {
+  // ---- host-side validation: nothing is launched on failure
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || T <= 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+  if ((flags & ~static_cast<unsigned>(FA_FLAG_TEST_STARVE_Q)) != 0u) return FA_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long n_qt = (static_cast<long long>(T) + 127) / 128;
+  const long long n_pairs = (n_qt + 1) / 2;
+  if (BH > INT32_MAX || n_pairs * BH > INT32_MAX) return FA_ERR_INVALID_ARG;
+  const long long elems = BH * T * d;
+  if (elems >= (1LL << 62) / 2) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * d * 2 >= (1LL << 40)) return FA_ERR_INVALID_ARG;  // TMA stride limit
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  const size_t tbytes = static_cast<size_t>(elems) * 2;
+  const size_t lbytes = static_cast<size_t>(BH) * T * 4;
+  if (overlaps(o, tbytes, q, tbytes) || overlaps(o, tbytes, k, tbytes) ||
+      overlaps(o, tbytes, v, tbytes) || overlaps(lse, lbytes, q, tbytes) ||
+      overlaps(lse, lbytes, k, tbytes) || overlaps(lse, lbytes, v, tbytes) ||
+      overlaps(lse, lbytes, o, tbytes))
+    return FA_ERR_INVALID_ARG;
+
+  int dev = -1;
+  const int dst = check_device(&dev);
+  if (dst != FA_OK) return dst;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return FA_ERR_LAUNCH;
+
+  fa::FwdLaunch a;
+  if (!encode_map(enc, &a.tm_q, q, T, d, static_cast<int>(BH)) ||
+      !encode_map(enc, &a.tm_k, k, T, d, static_cast<int>(BH)) ||
+      !encode_map(enc, &a.tm_v, v, T, d, static_cast<int>(BH)))
+    return FA_ERR_INVALID_ARG;
+  a.p.o = static_cast<__nv_bfloat16*>(o);
+  a.p.lse = lse;
+  a.p.status = status;
+  a.p.T = T;
+  a.p.BH = static_cast<int>(BH);
+  a.p.n_pairs = static_cast<int>(n_pairs);
+  a.p.n_kv = static_cast<int>(n_qt);
+  a.p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  a.p.timeout_ns = timeout_ns ? timeout_ns : 2000000000ull;
+  a.p.flags = flags;
+  a.grid = static_cast<unsigned>(n_pairs * BH);
+  a.stream = static_cast<cudaStream_t>(stream);
+
+  const cudaError_t e =
+      (d == 64) ? fa::launch_fwd_d64(a, causal != 0) : fa::launch_fwd_d128(a, causal != 0);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T,
+           int d, int causal, float scale, void* stream) {
+  return fa_fwd_ex(q, k, v, o, lse, B, H, T, d, causal, scale, nullptr, 0ull, 0u, stream);
+}
+
+}  // extern "C"

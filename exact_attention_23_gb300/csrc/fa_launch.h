@@ -1,0 +1,23 @@
+// Internal interface between the host API (fa_api.cu) and the kernel instantiations
+// (fa_fwd_d64.cu, fa_fwd_d128.cu). Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+struct FwdLaunch {
+  CUtensorMap tm_q, tm_k, tm_v;
+  FwdParams p;
+  unsigned grid;
+  cudaStream_t stream;
+};
+
+// Each returns the CUDA error of the launch (cudaSuccess when enqueued).
+cudaError_t launch_fwd_d64(const FwdLaunch& a, bool causal);
+cudaError_t launch_fwd_d128(const FwdLaunch& a, bool causal);
+
+}  // namespace fa

@@ -1,0 +1,127 @@
+"""CPU tests of the C ABI's host side: the library loads, exports every symbol the header
+declares, and rejects bad arguments before launching anything. No GPU compute here."""
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import exact_attention_23_gb300 as fa
+from exact_attention_23_gb300 import _binding
+from tests import oracle_pins
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _header_functions():
+    with open(os.path.join(ROOT, "include", "fa.h"), encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_binding.LIB_PATH):
+        from exact_attention_23_gb300 import build
+        build.build()
+    return fa.lib()
+
+
+def test_header_declares_expected_api():
+    assert _header_functions() == sorted(_binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_strerror(lib):
+    assert "sm_103a" in fa.version()
+    for code in range(6):
+        assert fa.strerror(code)
+    assert fa.strerror(99) == "unknown status"
+
+
+def test_status_codes_match_header():
+    with open(os.path.join(ROOT, "include", "fa.h"), encoding="utf-8") as f:
+        text = f.read()
+    for name in ("FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_MISALIGNED", "FA_ERR_UNSUPPORTED_DEVICE",
+                 "FA_ERR_LAUNCH", "FA_ERR_TIMEOUT"):
+        m = re.search(rf"\b{name}\s*=\s*(\d+)", text)
+        assert m and int(m.group(1)) == getattr(fa, name), name
+    m = re.search(r"#define\s+FA_FLAG_TEST_STARVE_Q\s+(\d+)u", text)
+    assert m and int(m.group(1)) == fa.FA_FLAG_TEST_STARVE_Q
+
+
+# Fake, never-dereferenced device addresses: validation fails before any CUDA call.
+A = 0x7F0000000000
+SZ = 1 << 30
+
+
+def _call(q=A, k=A + SZ, v=A + 2 * SZ, o=A + 3 * SZ, lse=A + 4 * SZ, B=1, H=1, T=128, d=64,
+          causal=1, scale=0.125, flags=0):
+    return fa.fa_fwd_ex(q, k, v, o, lse, B, H, T, d, causal, scale, None, 0, flags, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(k=0), fa.FA_ERR_INVALID_ARG),
+    (dict(v=0), fa.FA_ERR_INVALID_ARG),
+    (dict(o=0), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=0), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(T=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=32), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_INVALID_ARG),
+    (dict(d=256), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-0.125), fa.FA_ERR_INVALID_ARG),
+    (dict(flags=2), fa.FA_ERR_INVALID_ARG),
+    (dict(q=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(o=A + 3 * SZ + 2), fa.FA_ERR_MISALIGNED),
+    (dict(lse=A + 4 * SZ + 4), fa.FA_ERR_MISALIGNED),
+    (dict(o=A), fa.FA_ERR_INVALID_ARG),                 # o aliases q
+    (dict(o=A + SZ + 4096), fa.FA_ERR_INVALID_ARG),     # o overlaps k
+    (dict(lse=A + 2 * SZ + 16), fa.FA_ERR_INVALID_ARG),  # lse overlaps v
+    (dict(B=1 << 16, H=1 << 15, T=1 << 16), fa.FA_ERR_INVALID_ARG),  # grid / size overflow
+])
+def test_host_validation_rejects_before_launch(lib, kw, want):
+    assert _call(**kw) == want
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="only meaningful on a machine without a CUDA device")
+def test_valid_call_without_device_reports_unsupported(lib):
+    assert _call() == fa.FA_ERR_UNSUPPORTED_DEVICE
+    assert fa.fa_fwd(A, A + SZ, A + 2 * SZ, A + 3 * SZ, A + 4 * SZ, 1, 1, 128, 64, 1, 0.125,
+                     None) == fa.FA_ERR_UNSUPPORTED_DEVICE
+
+
+def test_python_wrapper_rejects_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fwd(x, x, x)
+
+
+def test_flop_and_byte_counts():
+    # causal FLOPs are half of 4·B·H·T²·d; bytes read q,k,v and write o (bf16) + lse (fp32)
+    assert fa.flops(4, 12, 4096, 64, True) == 0.5 * 4 * 4 * 12 * 4096 ** 2 * 64
+    assert fa.flops(2, 16, 16384, 128, False) == 4 * 2 * 16 * 16384 ** 2 * 128
+    assert fa.hbm_bytes(4, 12, 512, 64) == 24768 * 512
+
+
+def test_tiling_arithmetic_matches_the_page():
+    """The page's grid of (Q blocks, batch·heads) with 64-row blocks gives 3072 programs
+    at B4 H12 T4096; the same helper sizes this library's 128-row tiles."""
+    facts = oracle_pins.load_page_facts()
+    assert fa.q_tiles(4096, 64) * 4 * 12 == facts["programs_b4_h12_t4096_block64"]
+    assert fa.q_tiles(1000) == 8 and fa.q_tiles(128) == 1 and fa.q_tiles(129) == 2
+    assert math.ceil(fa.q_tiles(4096) / 2) * 48 == 768
