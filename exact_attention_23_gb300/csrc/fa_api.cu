@@ -33,12 +33,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-constexpr int kMaxDevices = 64;
+using fa::kMaxDevices;
 // 0 = unknown, 1 = supported (cc 10.3), 2 = unsupported
 int g_dev_state[kMaxDevices];
+int g_dev_sms[kMaxDevices];
 std::mutex g_dev_mu;
 
-int check_device(int* dev_out) {
+int check_device(int* dev_out, int* sms_out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
     cudaGetLastError();
@@ -54,8 +55,15 @@ int check_device(int* dev_out) {
       cudaGetLastError();
       return FA_ERR_UNSUPPORTED_DEVICE;
     }
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FA_ERR_UNSUPPORTED_DEVICE;
+    }
+    g_dev_sms[dev] = sms;
     g_dev_state[dev] = (major == 10 && minor == 3) ? 1 : 2;
   }
+  *sms_out = g_dev_sms[dev];
   return g_dev_state[dev] == 1 ? FA_OK : FA_ERR_UNSUPPORTED_DEVICE;
 }
 
@@ -112,7 +120,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   const long long BH = static_cast<long long>(B) * H;
   const long long n_qt = (static_cast<long long>(T) + 127) / 128;
   const long long n_pairs = (n_qt + 1) / 2;
-  if (BH > INT32_MAX || n_pairs * BH > INT32_MAX) return FA_ERR_INVALID_ARG;
+  if (BH > INT32_MAX || n_qt * BH > INT32_MAX) return FA_ERR_INVALID_ARG;
   const long long elems = BH * T * d;
   if (elems >= (1LL << 62) / 2) return FA_ERR_INVALID_ARG;
   if (static_cast<long long>(T) * d * 2 >= (1LL << 40)) return FA_ERR_INVALID_ARG;  // TMA stride limit
@@ -126,8 +134,8 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
       overlaps(lse, lbytes, o, tbytes))
     return FA_ERR_INVALID_ARG;
 
-  int dev = -1;
-  const int dst = check_device(&dev);
+  int dev = -1, sms = 0;
+  const int dst = check_device(&dev, &sms);
   if (dst != FA_OK) return dst;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return FA_ERR_LAUNCH;
@@ -142,12 +150,17 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.p.status = status;
   a.p.T = T;
   a.p.BH = static_cast<int>(BH);
-  a.p.n_pairs = static_cast<int>(n_pairs);
+  // Two 128-row Q tiles per CTA let the softmax of one overlap the MMAs of the other;
+  // only when pairs would leave most SMs idle does one tile per CTA pay.
+  const int tiles = (n_pairs * BH * 2 < sms) ? 1 : 2;
+  const long long n_units = (tiles == 2) ? n_pairs : n_qt;
+  a.p.n_units = static_cast<int>(n_units);
+  a.p.tiles_per_cta = tiles;
   a.p.n_kv = static_cast<int>(n_qt);
   a.p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   a.p.timeout_ns = timeout_ns ? timeout_ns : 2000000000ull;
   a.p.flags = flags;
-  a.grid = static_cast<unsigned>(n_pairs * BH);
+  a.grid = static_cast<unsigned>(n_units * BH);
   a.stream = static_cast<cudaStream_t>(stream);
 
   const cudaError_t e =

@@ -1,4 +1,6 @@
 // Instantiations of the attention forward kernel for head dim 64.
+#include <atomic>
+
 #include "fa_launch.h"
 
 namespace fa {
@@ -7,9 +9,16 @@ template <int D, bool CAUSAL>
 static cudaError_t launch_one(const FwdLaunch& a) {
   auto* fn = &fa_fwd_kernel<D, CAUSAL>;
   const int smem = Cfg<D>::kSmemBytes;
-  // Idempotent and cheap; done per call so that every device a caller uses is covered.
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
+  // The shared-memory opt-in is a per-device attribute: set it once per device.
+  static std::atomic<uint64_t> done[kMaxDevices / 64 + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const uint64_t bit = 1ull << (dev % 64);
+  if (!(done[dev / 64].load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    done[dev / 64].fetch_or(bit, std::memory_order_acq_rel);
+  }
   fn<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
   return cudaGetLastError();
 }

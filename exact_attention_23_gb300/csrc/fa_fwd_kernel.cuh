@@ -11,27 +11,41 @@
 // element. Scores use base 2 with log2(e)·scale folded into one factor (step ④, "exp2
 // and 1.4427"); the row logsumexp is emitted in natural log.
 //
-// One CTA = one (batch·head, pair of 128-row Q tiles). 320 threads, 10 warps:
+// One CTA = one (batch·head, pair of 128-row Q tiles). 352 threads, 11 warps:
 //   warps 0-3  softmax warpgroup for Q tile 0 (thread t owns query row t, TMEM lane t)
 //   warps 4-7  softmax warpgroup for Q tile 1
-//   warp  8    MMA issuer (one thread) and TMEM owner
-//   warp  9    TMA producer (one thread)
+//   warp  8    S issuer: S_i = Q_i·Kᵀ MMAs (one elected thread); TMEM owner
+//   warp  9    TMA producer
+//   warp 10    P·V issuer: O_i += P_i·V MMAs (one elected thread)
+// The two issuers run independently so that neither's barrier waits leave the tensor
+// core idle: a tcgen05.mma batch that starts on an idle tensor pipe pays several hundred
+// cycles of start-up, so the pipe is kept fed from two queues.
 // Tensor memory (512 columns × 128 lanes × 32 bit):
-//   [0,128)    S0 = Q0·Kᵀ (fp32), later overwritten by P0 (bf16 pairs, columns 0-63)
-//   [128,256)  S1 / P1
+//   [0,128)          S0 = Q0·Kᵀ (fp32)
+//   [128,256)        S1
 //   [256,256+D)      O0 (fp32 accumulator)
 //   [256+D,256+2D)   O1
+//   D = 64:  [384,448) P0, [448,512) P1 (bf16 pairs). Because P has its own columns, the
+//            next S = Q·Kᵀ is issued as soon as the softmax has read the current S into
+//            registers, and runs on the tensor core while that softmax is still working.
+//   D = 128: no room: P_i overwrites the first 64 columns of S_i, so the next S_i waits
+//            until P_i·V has consumed P_i.
 // The two Q tiles ping-pong: while one softmax warpgroup turns its S into P, the tensor
 // core computes the other tile's S or P·V.
 #pragma once
 
 #include "sm103.cuh"
 
+// Timeline hooks: compiled out unless a tracing build defines FA_TRACE(tag, step).
+#ifndef FA_TRACE
+#define FA_TRACE(tag, step) ((void)0)
+#endif
+
 namespace fa {
 
 constexpr int kBlockM = 128;    // query rows per Q tile = TMEM lanes
 constexpr int kBlockN = 128;    // keys per K/V tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr float kTau = 8.0f;    // lazy rescale: O and l keep a stale max until it is 2^8 too small
 constexpr uint32_t kFlagStarveQ = 1u;  // FA_FLAG_TEST_STARVE_Q
 
@@ -47,16 +61,24 @@ struct Cfg {
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + 1 KB alignment slack
+  // Tensor-memory columns (see the layout at the top of this file).
+  static constexpr bool kSepP = (D == 64);
+  static __device__ __forceinline__ constexpr uint32_t col_s(int i) { return i ? 128u : 0u; }
+  static __device__ __forceinline__ constexpr uint32_t col_o(int i) { return 256u + (i ? D : 0u); }
+  static __device__ __forceinline__ constexpr uint32_t col_p(int i) {
+    return kSepP ? (i ? 448u : 384u) : col_s(i);
+  }
 };
 
 struct Bars {
   uint64_t q_full;
   uint64_t k_full[4];
   uint64_t v_full[4];
-  uint64_t kv_empty[4];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_full[2];
+  uint64_t kv_empty[4];   // two arrivals per use: K released by the S issuer, V by the P·V issuer
+  uint64_t s_full[2];   // S_i computed (tensor core -> softmax)
+  uint64_t s_free[2];   // S_i read into registers (softmax -> MMA issuer); D = 64 only
+  uint64_t p_full[2];   // P_i stored, O_i rescaled if needed (softmax -> MMA issuer)
+  uint64_t pv_done[2];  // P_i·V done: P_i reusable, O_i stable (tensor core -> softmax)
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort;
@@ -70,8 +92,9 @@ struct FwdParams {
   int* status;
   int T;
   int BH;
-  int n_pairs;     // ceil(ceil(T/128)/2)
-  int n_kv;        // ceil(T/128)
+  int n_units;     // Q-tile groups per (batch, head): ceil(n_kv / tiles_per_cta)
+  int n_kv;        // ceil(T/128): K/V tiles, also Q tiles
+  int tiles_per_cta;  // 2 (ping-pong pair) or 1 (short sequences: more CTAs)
   float scale_log2;  // scale · log2(e)
   uint64_t timeout_ns;
   uint32_t flags;
@@ -91,17 +114,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31);
 
-  // Heavy-first order: the first CTAs launched take the last Q-tile pairs, which under
-  // the causal mask scan the most K/V tiles.
+  // Head-major order, heaviest Q tiles of a head first: CTAs resident together read the
+  // K/V of one or two heads (which then stay in L2), and under the causal mask the long
+  // scans start first while the short ones fill the tail.
   const int L = static_cast<int>(blockIdx.x);
-  const int pair = p.n_pairs - 1 - L / p.BH;
-  const int bh = L % p.BH;
-  const int qt0 = 2 * pair;
+  const int bh = L / p.n_units;
+  const int unit = p.n_units - 1 - L % p.n_units;
+  const int qt0 = unit * p.tiles_per_cta;
   int nkv[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int qt = qt0 + i;
-    nkv[i] = (qt * kBlockM >= p.T) ? 0 : (CAUSAL ? qt + 1 : p.n_kv);
+    nkv[i] = (i >= p.tiles_per_cta || qt * kBlockM >= p.T) ? 0 : (CAUSAL ? qt + 1 : p.n_kv);
   }
   const int n_steps = max(nkv[0], nkv[1]);
 
@@ -111,15 +135,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 4; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->kv_empty[s], 2);
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_free[i], 4);
       mbar_init(&bars->p_full[i], 4);
-      mbar_init(&bars->o_full[i], 1);
+      mbar_init(&bars->pv_done[i], 1);
     }
-    mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->mma_done, 2);
     bars->abort = 0u;
     bars->never = 0u;
     fence_mbar_init();
@@ -136,26 +161,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    // The whole warp runs the loop (uniform control flow); lane 0 issues the copies.
+    const bool leader = lane == 0;
+    if (leader) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const uint64_t keep = policy_evict_last();  // K/V are re-read by this head's other Q tiles
-      const bool load_q = (p.flags & kFlagStarveQ) == 0u;
-      if (load_q) {
-        mbar_arrive_expect_tx(&bars->q_full, 2 * C::kTileBytes);
+    }
+    const uint64_t keep = policy_evict_last();  // K/V are re-read by this head's other Q tiles
+    const bool load_q = (p.flags & kFlagStarveQ) == 0u;
+    if (load_q && leader) {
+      mbar_arrive_expect_tx(&bars->q_full, p.tiles_per_cta * C::kTileBytes);
+      for (int i = 0; i < p.tiles_per_cta; ++i)
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
-#pragma unroll
-          for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(smem + C::kQOff + i * C::kTileBytes + s * C::kSubBytes, &tm_q,
-                        &bars->q_full, s * 64, (qt0 + i) * kBlockM, bh);
-      }
-      int j = 0;
-      for (; j < n_steps; ++j) {
-        const int st = j % C::kStages;
-        const int use = j / C::kStages;
-        if (use > 0 && !mbar_wait(&bars->kv_empty[st], (use - 1) & 1, wc)) break;
+        for (int s = 0; s < C::kSub; ++s)
+          tma_load_3d(smem + C::kQOff + i * C::kTileBytes + s * C::kSubBytes, &tm_q,
+                      &bars->q_full, s * 64, (qt0 + i) * kBlockM, bh);
+    }
+    int j = 0;
+    for (; j < n_steps; ++j) {
+      const int st = j % C::kStages;
+      const int use = j / C::kStages;
+      if (use > 0 && !mbar_wait_warp(&bars->kv_empty[st], (use - 1) & 1, wc)) break;
+      FA_TRACE(1, j);
+      if (leader) {
         mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
 #pragma unroll
         for (int s = 0; s < C::kSub; ++s)
@@ -167,96 +196,108 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d_hint(smem + C::kVOff + st * C::kTileBytes + s * C::kSubBytes, &tm_v,
                            &bars->v_full[st], s * 64, j * kBlockN, bh, keep);
       }
-      // Drain: every copy issued must have landed before this CTA may exit.
-      const WaitCtl drain{&bars->never, nullptr, p.timeout_ns};
-      if (load_q) mbar_wait(&bars->q_full, 0, drain);
-      const int issued = j;
-      for (int st = 0; st < C::kStages && st < issued; ++st) {
-        const int last_use = (issued - 1 - st) / C::kStages;
-        mbar_wait(&bars->k_full[st], last_use & 1, drain);
-        mbar_wait(&bars->v_full[st], last_use & 1, drain);
-      }
+      __syncwarp();
     }
-  } else if (warp == 8) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // Drain: every copy issued must have landed before this CTA may exit.
+    const WaitCtl drain{&bars->never, nullptr, p.timeout_ns};
+    if (load_q) mbar_wait_warp(&bars->q_full, 0, drain);
+    const int issued = j;
+    for (int st = 0; st < C::kStages && st < issued; ++st) {
+      const int last_use = (issued - 1 - st) / C::kStages;
+      mbar_wait_warp(&bars->k_full[st], last_use & 1, drain);
+      mbar_wait_warp(&bars->v_full[st], last_use & 1, drain);
+    }
+  } else if (warp == 8 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // The whole warp runs the schedule and waits (uniform control flow); lane 0 alone
+    // issues each batch of tcgen05.mma and the commit that tracks it.
+    const bool leader = lane == 0;
+    const WaitCtl drain{&bars->never, nullptr, p.timeout_ns};
+    auto commit = [&](uint64_t* bar) {
+      if (leader) mma_commit(bar);
+      __syncwarp();
+    };
+    if (warp == 8) {
+      // S_i = Q_i · K_stᵀ : M=128, N=128, K=D in steps of 16 (32 bytes inside a 128-byte
+      // swizzled row; a new 16 KB box every 64 columns). Committed to s_full[i].
       constexpr uint32_t kIdescS = idesc_bf16(kBlockM, kBlockN, false);
-      constexpr uint32_t kIdescO = idesc_bf16(kBlockM, D, true);
       const uint32_t q_base = smem_u32(smem + C::kQOff);
       const uint32_t k_base = smem_u32(smem + C::kKOff);
-      const uint32_t v_base = smem_u32(smem + C::kVOff);
-      const uint32_t t_s[2] = {tmem + 0u, tmem + 128u};
-      const uint32_t t_o[2] = {tmem + 256u, tmem + 256u + static_cast<uint32_t>(D)};
-
-      // S_i = Q_i · K_stᵀ : M=128, N=128, K=D in steps of 16 (32 bytes inside a 128-byte
-      // swizzled row; a new 16 KB box every 64 columns).
       auto issue_s = [&](int i, int st) {
-        const uint32_t qa = q_base + i * C::kTileBytes;
-        const uint32_t ka = k_base + st * C::kTileBytes;
+        if (leader) {
+          const uint32_t qa = q_base + i * C::kTileBytes;
+          const uint32_t ka = k_base + st * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kSubBytes + (kk & 3) * 32;
-          mma_ss(t_s[i], sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                 kIdescS, kk > 0 ? 1u : 0u);
-        }
-      };
-      // O_i += P_i · V_st : A = P from TMEM (8 columns = 16 keys per step), B = V tile,
-      // MN-major (D contiguous): 16 keys = 2048 bytes per step; next 64-wide column block
-      // (leading byte offset) 16 KB away; next 8-key group (stride byte offset) 1 KB away.
-      auto issue_pv = [&](int i, int st, bool acc) {
-        const uint32_t va = v_base + st * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          mma_ts(t_o[i], t_s[i] + kk * 8, sdesc_sw128(va + kk * 2048, C::kSubBytes, 1024),
-                 kIdescO, (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-
-      bool ok = n_steps > 0 && mbar_wait(&bars->q_full, 0, wc) && mbar_wait(&bars->k_full[0], 0, wc);
-      if (ok) {
-        tc_fence_after_sync();
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-          if (nkv[i] > 0) {
-            issue_s(i, 0);
-            mma_commit(&bars->s_full[i]);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kSubBytes + (kk & 3) * 32;
+            mma_ss(tmem + C::col_s(i), sdesc_sw128(qa + off, 16, 1024),
+                   sdesc_sw128(ka + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
           }
-      }
+          mma_commit(&bars->s_full[i]);
+        }
+        __syncwarp();
+      };
+      bool ok = n_steps > 0 && mbar_wait_warp(&bars->q_full, 0, wc);
       for (int j = 0; ok && j < n_steps; ++j) {
         const int st = j % C::kStages;
-        if (!mbar_wait(&bars->v_full[st], (j / C::kStages) & 1, wc)) { ok = false; break; }
-        const int st_next = (j + 1) % C::kStages;
-        bool k_next_ready = false;
+        if (!mbar_wait_warp(&bars->k_full[st], (j / C::kStages) & 1, wc)) { ok = false; break; }
+        tc_fence_after_sync();
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (j >= nkv[i]) continue;
-          if (!mbar_wait(&bars->p_full[i], j & 1, wc)) { ok = false; break; }
-          tc_fence_after_sync();
-          issue_pv(i, st, j > 0);
-          if (j + 1 < nkv[i]) {
-            if (!k_next_ready) {
-              if (!mbar_wait(&bars->k_full[st_next], ((j + 1) / C::kStages) & 1, wc)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after_sync();
-              k_next_ready = true;
-            }
-            issue_s(i, st_next);
-            mma_commit(&bars->s_full[i]);
-          } else {
-            mma_commit(&bars->o_full[i]);
+          if (j > 0) {
+            // S_i may be overwritten once its softmax has read it (P in its own columns)
+            // or, when P_i lives in S_i's columns, once P_i·V has consumed P_i.
+            uint64_t* freed = C::kSepP ? &bars->s_free[i] : &bars->pv_done[i];
+            if (!mbar_wait_warp(freed, (j - 1) & 1, wc)) { ok = false; break; }
+            tc_fence_after_sync();
           }
+          issue_s(i, st);
+          FA_TRACE(16 + i, j);
         }
         if (!ok) break;
-        mma_commit(&bars->kv_empty[st]);
+        commit(&bars->kv_empty[st]);  // K_j is free once these S MMAs are done
       }
-      // Nothing may still be running on the tensor core when TMEM is released.
-      mma_commit(&bars->mma_done);
-      const WaitCtl drain{&bars->never, nullptr, p.timeout_ns};
-      mbar_wait(&bars->mma_done, 0, drain);
+    } else {
+      // O_i += P_i · V_st : A = P from TMEM (8 columns = 16 keys per step), B = V tile,
+      // MN-major (D contiguous): 16 keys = 2048 bytes per step; next 64-wide column block
+      // (leading byte offset) 16 KB away; next 8-key group (stride byte offset) 1 KB away.
+      // Committed to pv_done[i].
+      constexpr uint32_t kIdescO = idesc_bf16(kBlockM, D, true);
+      const uint32_t v_base = smem_u32(smem + C::kVOff);
+      auto issue_pv = [&](int i, int st, bool acc) {
+        if (leader) {
+          const uint32_t va = v_base + st * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBlockN / 16; ++kk) {
+            mma_ts(tmem + C::col_o(i), tmem + C::col_p(i) + kk * 8,
+                   sdesc_sw128(va + kk * 2048, C::kSubBytes, 1024), kIdescO,
+                   (acc || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars->pv_done[i]);
+        }
+        __syncwarp();
+      };
+      bool ok = n_steps > 0;
+      for (int j = 0; ok && j < n_steps; ++j) {
+        const int st = j % C::kStages;
+        if (!mbar_wait_warp(&bars->v_full[st], (j / C::kStages) & 1, wc)) { ok = false; break; }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (j >= nkv[i]) continue;
+          if (!mbar_wait_warp(&bars->p_full[i], j & 1, wc)) { ok = false; break; }
+          FA_TRACE(11 + i, j);
+          tc_fence_after_sync();
+          issue_pv(i, st, j > 0);
+          FA_TRACE(14 + i, j);
+        }
+        if (!ok) break;
+        commit(&bars->kv_empty[st]);  // V_j is free once these P·V MMAs are done
+      }
     }
-    __syncwarp();
+    // Nothing may still be running on the tensor core when TMEM is released.
+    commit(&bars->mma_done);
+    mbar_wait_warp(&bars->mma_done, 0, drain);
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     const int wg = warp >> 2;
@@ -266,8 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q_row = qt * kBlockM + row;
     const int n = nkv[wg];
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + static_cast<uint32_t>(wg * 128);
-    const uint32_t t_o = tmem + lane_off + 256u + static_cast<uint32_t>(wg * D);
+    const uint32_t t_s = tmem + lane_off + C::col_s(wg);
+    const uint32_t t_o = tmem + lane_off + C::col_o(wg);
+    const uint32_t t_p = tmem + lane_off + C::col_p(wg);
     const float c = p.scale_log2;
 
     float m_ref = -INFINITY;  // reference max (base-2 scaled units) shared by O and l
@@ -275,32 +317,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       if (!mbar_wait_warp(&bars->s_full[wg], j & 1, wc)) { ok = false; break; }
+      FA_TRACE(30 + wg, j);
       tc_fence_after_sync();
-      uint32_t s[kBlockN];
-#pragma unroll
-      for (int c0 = 0; c0 < kBlockN; c0 += 32) tmem_ld32(t_s + c0, s + c0);
-      tmem_ld_wait();
-#pragma unroll
-      for (int c0 = 0; c0 < kBlockN; c0 += 32) reg_fence32(s + c0);
-
       const int k0 = j * kBlockN;
-      const bool diag = CAUSAL && (j == qt);
-      if (diag || k0 + kBlockN > p.T) {
-        // Keys past the end of the sequence, and (diagonal tile) keys after this query.
-        const int lim = (CAUSAL ? min(q_row + 1, p.T) : p.T) - k0;
+      const bool masked = (CAUSAL && j == qt) || (k0 + kBlockN > p.T);
+      // Keys past the end of the sequence, and (diagonal tile) keys after this query.
+      const int lim = (CAUSAL ? min(q_row + 1, p.T) : p.T) - k0;
+
+      // S in two halves: the second half loads while the first is masked and maxed.
+      uint32_t s[kBlockN];
+      tmem_ld32(t_s + 0, s);
+      tmem_ld32(t_s + 32, s + 32);
+      tmem_ld_wait();
+      reg_fence32(s);
+      reg_fence32(s + 32);
+      tmem_ld32(t_s + 64, s + 64);
+      tmem_ld32(t_s + 96, s + 96);
+      if (masked) {
 #pragma unroll
-        for (int t = 0; t < kBlockN; ++t)
+        for (int t = 0; t < 64; ++t)
           if (t >= lim) s[t] = __float_as_uint(-INFINITY);
       }
-      float mx0 = u2f(s[0]), mx1 = u2f(s[1]), mx2 = u2f(s[2]), mx3 = u2f(s[3]);
+      float mx[8];
 #pragma unroll
-      for (int t = 4; t < kBlockN; t += 4) {
-        mx0 = fmaxf(mx0, u2f(s[t]));
-        mx1 = fmaxf(mx1, u2f(s[t + 1]));
-        mx2 = fmaxf(mx2, u2f(s[t + 2]));
-        mx3 = fmaxf(mx3, u2f(s[t + 3]));
+      for (int a = 0; a < 8; ++a) mx[a] = fmaxf(u2f(s[2 * a]), u2f(s[2 * a + 1]));
+#pragma unroll
+      for (int t = 16; t < 64; t += 16)
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx[a] = fmax3(mx[a], u2f(s[t + 2 * a]), u2f(s[t + 2 * a + 1]));
+      tmem_ld_wait();
+      reg_fence32(s + 64);
+      reg_fence32(s + 96);
+      if constexpr (C::kSepP) {
+        // S_i is in registers: the tensor core may overwrite it with the next S_i.
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free[wg]);
       }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      FA_TRACE(20 + wg, j);
+      if (masked) {
+#pragma unroll
+        for (int t = 64; t < kBlockN; ++t)
+          if (t >= lim) s[t] = __float_as_uint(-INFINITY);
+      }
+#pragma unroll
+      for (int t = 64; t < kBlockN; t += 16)
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx[a] = fmax3(mx[a], u2f(s[t + 2 * a]), u2f(s[t + 2 * a + 1]));
+      const float m_tile =
+          fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c;
+      FA_TRACE(40 + wg, j);
 
       float alpha = 1.0f;
       bool rescale = false;
@@ -313,26 +379,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         rescale = true;
       }
 
-      const float neg_m = -m_ref;
-      float ls0 = 0.f, ls1 = 0.f;
+      // p = 2^(s·c − m_ref) on fp32 pairs; row sum in fp32; P kept as bf16 pairs.
+      const uint64_t c2 = f2_pack(c, c);
+      const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
+      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+      uint32_t pk[kBlockN / 2];
 #pragma unroll
-      for (int c0 = 0; c0 < kBlockN; c0 += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const float p0 = ex2_approx(fmaf(u2f(s[c0 + 2 * t]), c, neg_m));
-          const float p1 = ex2_approx(fmaf(u2f(s[c0 + 2 * t + 1]), c, neg_m));
-          ls0 += p0;
-          ls1 += p1;
-          pk[t] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(t_s + static_cast<uint32_t>(c0 / 2), pk);
+      for (int t = 0; t < kBlockN / 2; ++t) {
+        const uint64_t x2 = f2_fma(f2_pack(u2f(s[2 * t]), u2f(s[2 * t + 1])), c2, nm2);
+        float x0, x1;
+        f2_unpack(x2, x0, x1);
+        const float p0 = ex2_approx(x0);
+        const float p1 = ex2_approx(x1);
+        if (t & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
+        else acc0 = f2_add(acc0, f2_pack(p0, p1));
+        pk[t] = pack_bf16x2(p0, p1);
       }
-      l += ls0 + ls1;
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(acc0, a0, a1);
+        f2_unpack(acc1, b0, b1);
+        l += (a0 + b0) + (a1 + b1);
+      }
+      FA_TRACE(42 + wg, j);
+      if constexpr (C::kSepP) {
+        // P_i's columns and O_i are free once the previous P_i·V has finished.
+        if (j > 0) {
+          if (!mbar_wait_warp(&bars->pv_done[wg], (j - 1) & 1, wc)) { ok = false; break; }
+          tc_fence_after_sync();
+        }
+      }
       if (__any_sync(0xffffffffu, rescale)) {
-        // Rows whose max jumped bring their accumulated O to the new reference (done
-        // after P is written, when the score registers are free; O is not read by the
-        // tensor core until this warp arrives on p_full below).
+        // Rows whose max jumped bring their accumulated O to the new reference. O is
+        // stable here (the previous P·V is done) and not read again before p_full.
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t r[32];
@@ -344,14 +423,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(t_o + c0, r);
         }
       }
+      tmem_st32(t_p + 0, pk);
+      tmem_st32(t_p + 32, pk + 32);
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->p_full[wg]);
+      FA_TRACE(22 + wg, j);
     }
 
     if (n > 0) {
-      const bool good = ok && mbar_wait_warp(&bars->o_full[wg], 0, wc);
+      const bool good = ok && mbar_wait_warp(&bars->pv_done[wg], (n - 1) & 1, wc);
+      FA_TRACE(24 + wg, 0);
       const size_t row_idx = static_cast<size_t>(bh) * static_cast<size_t>(p.T) +
                              static_cast<size_t>(q_row);
       const bool in_range = q_row < p.T;
@@ -366,16 +449,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           reg_fence32(r);
           if (in_range) {
-            uint32_t pk[16];
+            uint32_t ob[16];
 #pragma unroll
             for (int t = 0; t < 16; ++t)
-              pk[t] = pack_bf16x2(u2f(r[2 * t]) * inv_l, u2f(r[2 * t + 1]) * inv_l);
+              ob[t] = pack_bf16x2(u2f(r[2 * t]) * inv_l, u2f(r[2 * t + 1]) * inv_l);
 #pragma unroll
             for (int t = 0; t < 4; ++t)
-              orow[c0 / 8 + t] = make_uint4(pk[4 * t], pk[4 * t + 1], pk[4 * t + 2], pk[4 * t + 3]);
+              orow[c0 / 8 + t] = make_uint4(ob[4 * t], ob[4 * t + 1], ob[4 * t + 2], ob[4 * t + 3]);
           }
         }
         if (in_range) p.lse[row_idx] = (m_ref + log2f(l)) * 0.69314718055994530942f;
+        FA_TRACE(26 + wg, 0);
       } else if (in_range) {
         const uint32_t nan2 = 0x7FC07FC0u;  // two bf16 quiet NaNs
 #pragma unroll

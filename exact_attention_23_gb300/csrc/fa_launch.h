@@ -9,6 +9,8 @@
 
 namespace fa {
 
+constexpr int kMaxDevices = 64;
+
 struct FwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v;
   FwdParams p;

@@ -68,6 +68,10 @@ struct WaitCtl {
 constexpr int kErrTimeout = 5;  // equals FA_ERR_TIMEOUT in fa.h
 
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, WaitCtl w) {
+  // try_wait itself suspends the thread for a short while, so plain polling costs no
+  // issue slots; the timer is only read once a wait is already long.
+  for (int i = 0; i < 4096; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -84,17 +88,41 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 
 // Single-thread bounded wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
-  if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+  for (int i = 0; i < 16; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, w);
 }
 
-// Whole-warp bounded wait with a warp-uniform answer (needed before .sync.aligned
-// tcgen05 instructions): lane 0 waits, the verdict is broadcast.
+// Whole-warp bounded wait with a warp-uniform answer: every lane polls and lane 0's
+// view is broadcast, so the warp never diverges around a wait (divergent control flow
+// in the issuing warps costs far more than the poll itself).
+static __device__ __noinline__ bool mbar_wait_warp_slow(uint64_t* bar, uint32_t parity, WaitCtl w) {
+  for (int i = 0; i < 4096; ++i)
+    if (__shfl_sync(0xffffffffu, mbar_try_wait(bar, parity) ? 1u : 0u, 0)) return true;
+  uint64_t t0 = global_timer_ns();
+  t0 = __shfl_sync(0xffffffffu, t0, 0);
+  for (uint32_t it = 1;; ++it) {
+    if (__shfl_sync(0xffffffffu, mbar_try_wait(bar, parity) ? 1u : 0u, 0)) return true;
+    if ((it & 63u) == 0u) {
+      uint32_t verdict = 0u;  // 1 = give up (another role aborted), 2 = timed out here
+      if ((threadIdx.x & 31u) == 0u) {
+        if (*w.abort) verdict = 1u;
+        else if (global_timer_ns() - t0 > w.timeout_ns) verdict = 2u;
+      }
+      verdict = __shfl_sync(0xffffffffu, verdict, 0);
+      if (verdict == 2u && (threadIdx.x & 31u) == 0u) {
+        *w.abort = 1u;
+        if (w.status) atomicExch(w.status, kErrTimeout);
+      }
+      if (verdict != 0u) return false;
+    }
+  }
+}
+
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
-  uint32_t ok = 0;
-  if ((threadIdx.x & 31u) == 0u) ok = mbar_wait(bar, parity, w) ? 1u : 0u;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  return ok != 0u;
+  if (__shfl_sync(0xffffffffu, mbar_try_wait(bar, parity) ? 1u : 0u, 0)) return true;
+  return mbar_wait_warp_slow(bar, parity, w);
 }
 
 // ------------------------------------------------------------------------------------
@@ -286,6 +314,34 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Three-input fp32 maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed pairs of fp32 in one 64-bit register: {lo, hi}.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+// Elementwise a*b + c and a + b on fp32 pairs (one instruction each on sm_100 and later).
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` lands in bits 0-15.
