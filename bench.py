@@ -116,6 +116,32 @@ class ClockSampler:
                 "power_w_max": pmax, "reasons": sorted(reasons)}
 
 
+def _kernel_source_sha256() -> str:
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "exact_attention_23_gb300", "csrc", "*"))):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(os.path.basename(f).encode())
+            with open(f, "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()
+
+
+def _measured_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu record, or None
+    when the kernel sources changed after the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_fa_fwd_d64_causal_t16384.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("kernel_source_sha256") != _kernel_source_sha256():
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
 def _smi_index(cuda_index: int) -> str:
     """nvidia-smi names GPUs by physical index or UUID; map through CUDA_VISIBLE_DEVICES."""
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
@@ -134,13 +160,22 @@ def _dist():
 
 
 def _max_over_ranks(x: float, ws: int) -> float:
+    """Slowest rank's value (the timing convention for N > 1); host-side plumbing only."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_tflops(flops_per_step: float, steps: int, elapsed_ms_local: float, ws: int):
+    """Whole-job throughput: every rank does `flops_per_step` per step (independent replicas),
+    the job takes as long as its slowest rank. Returns (TFLOP/s, max elapsed ms)."""
+    elapsed = _max_over_ranks(elapsed_ms_local, ws)
+    return ws * flops_per_step * steps / (elapsed * 1e-3) / 1e12, elapsed
 
 
 def _barrier(ws: int):
@@ -277,8 +312,7 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     _barrier(ws)
     clocks = sampler.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    elapsed_ms = _max_over_ranks(elapsed_ms, ws)
+    value, elapsed_ms = aggregate_tflops(flops_step, args.steps, t_start.elapsed_time(t_end), ws)
     launches = args.steps * len(sets)
 
     bf16_peak, bf16_sus, hbm_peak, peak_kind = _peaks()
@@ -292,7 +326,6 @@ def run_gpu(args):
                       "frac_of_sustained": fl / ms / 1e9 / bf16_sus,
                       "gbs": by / ms / 1e6, "frac_hbm": by / ms / 1e6 / hbm_peak})
     dom = max(per_T, key=lambda r: fa.flops(B, H, r["T"], D, True))
-    value = ws * flops_step * args.steps / (elapsed_ms * 1e-3) / 1e12
 
     # ---- end to end: pinned host inputs -> device -> forward -> host, per step
     e2e_steps = max(1, min(args.steps, 10))
@@ -321,8 +354,7 @@ def run_gpu(args):
             hl.copy_(lse, non_blocking=True)
     e_end.record(stream)
     torch.cuda.synchronize(dev)
-    e_ms = _max_over_ranks(e_start.elapsed_time(e_end), ws)
-    e2e_value = ws * flops_step * e2e_steps / (e_ms * 1e-3) / 1e12
+    e2e_value, e_ms = aggregate_tflops(flops_step, e2e_steps, e_start.elapsed_time(e_end), ws)
 
     result = None
     if rank == 0:
@@ -346,7 +378,9 @@ def run_gpu(args):
             "per_T": per_T,
             "roofline": {"bound": "tensor", "achieved": dom["tflops"], "peak": bf16_sus,
                          "unit": "TFLOP/s", "frac": dom["tflops"] / bf16_sus,
-                         "traffic": args.traffic,
+                         "traffic": args.traffic if args.traffic is not None else (
+                             _measured_traffic() if dom["T"] == 16384 else None),
+                         "algorithmic_bytes": fa.hbm_bytes(B, H, dom["T"], D),
                          "kernel": f"fa_fwd_kernel<64,causal> at T={dom['T']} "
                                    f"({fa.flops(B, H, dom['T'], D, True):.4g} FLOP per launch; "
                                    f"peak = {peak_kind} sustained bf16)"},
