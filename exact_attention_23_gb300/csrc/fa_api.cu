@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -155,12 +156,15 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   const int tiles = (n_pairs * BH * 2 < sms) ? 1 : 2;
   const long long n_units = (tiles == 2) ? n_pairs : n_qt;
   a.p.n_units = static_cast<int>(n_units);
+  a.p.total_units = static_cast<int>(n_units * BH);
   a.p.tiles_per_cta = tiles;
   a.p.n_kv = static_cast<int>(n_qt);
   a.p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   a.p.timeout_ns = timeout_ns ? timeout_ns : 2000000000ull;
   a.p.flags = flags;
-  a.grid = static_cast<unsigned>(n_units * BH);
+  // Persistent: one CTA per SM (at most one per unit); each walks units blockIdx.x,
+  // blockIdx.x + gridDim.x, ...
+  a.grid = static_cast<unsigned>(std::min<long long>(n_units * BH, sms));
   a.stream = static_cast<cudaStream_t>(stream);
 
   const cudaError_t e =

@@ -11,7 +11,10 @@
 // element. Scores use base 2 with log2(e)·scale folded into one factor (step ④, "exp2
 // and 1.4427"); the row logsumexp is emitted in natural log.
 //
-// One CTA = one (batch·head, pair of 128-row Q tiles). 352 threads, 11 warps:
+// Work unit = one (batch·head, pair of 128-row Q tiles). The kernel is persistent: one
+// CTA per SM walks a strided list of units, so that the next unit's Q/K/V loads and first
+// S = Q·Kᵀ overlap the current unit's epilogue, and TMEM/barrier set-up happens once.
+// 352 threads, 11 warps:
 //   warps 0-3  softmax warpgroup for Q tile 0 (thread t owns query row t, TMEM lane t)
 //   warps 4-7  softmax warpgroup for Q tile 1
 //   warp  8    S issuer: S_i = Q_i·Kᵀ MMAs (one elected thread); TMEM owner
@@ -30,8 +33,9 @@
 //            registers, and runs on the tensor core while that softmax is still working.
 //   D = 128: no room: P_i overwrites the first 64 columns of S_i, so the next S_i waits
 //            until P_i·V has consumed P_i.
-// The two Q tiles ping-pong: while one softmax warpgroup turns its S into P, the tensor
-// core computes the other tile's S or P·V.
+// Every barrier phase is counted over the CTA's whole list of units (each role walks the
+// same list and keeps the same running counts), so units follow one another with no
+// re-initialisation.
 #pragma once
 
 #include "sm103.cuh"
@@ -53,11 +57,12 @@ template <int D>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kStages = (D == 64) ? 3 : 2;      // K/V ring depth (measured: 3 beats 2, 4 and 6 at d=64)
+  static constexpr int kQBufs = (D == 64) ? 2 : 1;       // Q tile pairs in flight (next unit's Q)
   static constexpr int kSubBytes = kBlockM * 64 * 2;     // one 128-row × 64-col bf16 box = 16 KB
   static constexpr int kSub = D / 64;                    // boxes per tile row-block
   static constexpr int kTileBytes = kSub * kSubBytes;    // a 128×D bf16 tile
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + 2 * kTileBytes;
+  static constexpr int kKOff = kQOff + kQBufs * 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + 1 KB alignment slack
@@ -71,14 +76,16 @@ struct Cfg {
 };
 
 struct Bars {
-  uint64_t q_full;
+  uint64_t q_full[2];   // a unit's Q tiles landed (producer -> S issuer)
+  uint64_t q_empty[2];  // the S issuer is done with a Q buffer (tensor core -> producer)
   uint64_t k_full[4];
   uint64_t v_full[4];
-  uint64_t kv_empty[4];   // two arrivals per use: K released by the S issuer, V by the P·V issuer
+  uint64_t kv_empty[4]; // two arrivals per use: K released by the S issuer, V by the P·V issuer
   uint64_t s_full[2];   // S_i computed (tensor core -> softmax)
-  uint64_t s_free[2];   // S_i read into registers (softmax -> MMA issuer); D = 64 only
-  uint64_t p_full[2];   // P_i stored, O_i rescaled if needed (softmax -> MMA issuer)
+  uint64_t s_free[2];   // S_i read into registers (softmax -> S issuer); D = 64 only
+  uint64_t p_full[2];   // P_i stored, O_i rescaled if needed (softmax -> P·V issuer)
   uint64_t pv_done[2];  // P_i·V done: P_i reusable, O_i stable (tensor core -> softmax)
+  uint64_t o_free[2];   // a unit's O_i has been read out (softmax -> P·V issuer)
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort;
@@ -92,15 +99,44 @@ struct FwdParams {
   int* status;
   int T;
   int BH;
-  int n_units;     // Q-tile groups per (batch, head): ceil(n_kv / tiles_per_cta)
-  int n_kv;        // ceil(T/128): K/V tiles, also Q tiles
+  int n_units;        // Q-tile groups per (batch, head): ceil(n_kv / tiles_per_cta)
+  int total_units;    // n_units · BH
+  int n_kv;           // ceil(T/128): K/V tiles, also Q tiles
   int tiles_per_cta;  // 2 (ping-pong pair) or 1 (short sequences: more CTAs)
-  float scale_log2;  // scale · log2(e)
+  float scale_log2;   // scale · log2(e)
   uint64_t timeout_ns;
   uint32_t flags;
 };
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+// One work unit. Units are numbered heaviest first (under the causal mask the cost of a
+// Q-tile pair grows with its position), all heads of one position together; CTA c takes
+// the units of round r = 0, 1, 2, ... at position c in even rounds and G−1−c in odd rounds
+// (G = grid size). Over a list sorted by cost this zig-zag gives every CTA nearly the same
+// total work without any shared counter.
+struct Unit {
+  int bh, qt0, nkv[2], n_steps;
+};
+
+__device__ __forceinline__ int unit_index(int round, int cta, int grid) {
+  return round * grid + ((round & 1) ? grid - 1 - cta : cta);
+}
+
+template <bool CAUSAL>
+__device__ __forceinline__ Unit unit_of(const FwdParams& p, int L) {
+  Unit u;
+  u.bh = L % p.BH;
+  const int idx = p.n_units - 1 - L / p.BH;
+  u.qt0 = idx * p.tiles_per_cta;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int qt = u.qt0 + i;
+    u.nkv[i] = (i >= p.tiles_per_cta || qt * kBlockM >= p.T) ? 0 : (CAUSAL ? qt + 1 : p.n_kv);
+  }
+  u.n_steps = max(u.nkv[0], u.nkv[1]);
+  return u;
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -113,24 +149,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31);
-
-  // Head-major order, heaviest Q tiles of a head first: CTAs resident together read the
-  // K/V of one or two heads (which then stay in L2), and under the causal mask the long
-  // scans start first while the short ones fill the tail.
-  const int L = static_cast<int>(blockIdx.x);
-  const int bh = L / p.n_units;
-  const int unit = p.n_units - 1 - L % p.n_units;
-  const int qt0 = unit * p.tiles_per_cta;
-  int nkv[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int qt = qt0 + i;
-    nkv[i] = (i >= p.tiles_per_cta || qt * kBlockM >= p.T) ? 0 : (CAUSAL ? qt + 1 : p.n_kv);
-  }
-  const int n_steps = max(nkv[0], nkv[1]);
+  const int cta = static_cast<int>(blockIdx.x);
+  const int grid = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->q_full, 1);
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->q_full[b], 1);
+      mbar_init(&bars->q_empty[b], 1);
+    }
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       mbar_init(&bars->k_full[s], 1);
@@ -143,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_free[i], 4);
       mbar_init(&bars->p_full[i], 4);
       mbar_init(&bars->pv_done[i], 1);
+      mbar_init(&bars->o_free[i], 4);
     }
     mbar_init(&bars->mma_done, 2);
     bars->abort = 0u;
@@ -158,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort, p.status, p.timeout_ns};
+  const WaitCtl drain{&bars->never, nullptr, p.timeout_ns};
 
   if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
@@ -170,40 +199,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint64_t keep = policy_evict_last();  // K/V are re-read by this head's other Q tiles
     const bool load_q = (p.flags & kFlagStarveQ) == 0u;
-    if (load_q && leader) {
-      mbar_arrive_expect_tx(&bars->q_full, p.tiles_per_cta * C::kTileBytes);
-      for (int i = 0; i < p.tiles_per_cta; ++i)
+    int g = 0;       // K/V steps issued so far (over this CTA's units)
+    int qn = 0;      // Q tile pairs issued so far
+    bool ok = true;
+    for (int r = 0; ok && r * grid < p.total_units; ++r) {
+      const int L = unit_index(r, cta, grid);
+      if (L >= p.total_units) continue;
+      const Unit u = unit_of<CAUSAL>(p, L);
+      const int qb = qn % C::kQBufs;
+      if (qn >= C::kQBufs &&
+          !mbar_wait_warp(&bars->q_empty[qb], ((qn / C::kQBufs) - 1) & 1, wc)) { ok = false; break; }
+      if (load_q && leader) {
+        mbar_arrive_expect_tx(&bars->q_full[qb], p.tiles_per_cta * C::kTileBytes);
+        for (int i = 0; i < p.tiles_per_cta; ++i)
 #pragma unroll
-        for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d(smem + C::kQOff + i * C::kTileBytes + s * C::kSubBytes, &tm_q,
-                      &bars->q_full, s * 64, (qt0 + i) * kBlockM, bh);
-    }
-    int j = 0;
-    for (; j < n_steps; ++j) {
-      const int st = j % C::kStages;
-      const int use = j / C::kStages;
-      if (use > 0 && !mbar_wait_warp(&bars->kv_empty[st], (use - 1) & 1, wc)) break;
-      FA_TRACE(1, j);
-      if (leader) {
-        mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
-#pragma unroll
-        for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d_hint(smem + C::kKOff + st * C::kTileBytes + s * C::kSubBytes, &tm_k,
-                           &bars->k_full[st], s * 64, j * kBlockN, bh, keep);
-        mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
-#pragma unroll
-        for (int s = 0; s < C::kSub; ++s)
-          tma_load_3d_hint(smem + C::kVOff + st * C::kTileBytes + s * C::kSubBytes, &tm_v,
-                           &bars->v_full[st], s * 64, j * kBlockN, bh, keep);
+          for (int s = 0; s < C::kSub; ++s)
+            tma_load_3d(smem + C::kQOff + (qb * 2 + i) * C::kTileBytes + s * C::kSubBytes, &tm_q,
+                        &bars->q_full[qb], s * 64, (u.qt0 + i) * kBlockM, u.bh);
       }
       __syncwarp();
+      ++qn;
+      for (int j = 0; j < u.n_steps; ++j, ++g) {
+        const int st = g % C::kStages;
+        const int use = g / C::kStages;
+        if (use > 0 && !mbar_wait_warp(&bars->kv_empty[st], (use - 1) & 1, wc)) { ok = false; break; }
+        FA_TRACE(1, j);
+        if (leader) {
+          mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
+#pragma unroll
+          for (int s = 0; s < C::kSub; ++s)
+            tma_load_3d_hint(smem + C::kKOff + st * C::kTileBytes + s * C::kSubBytes, &tm_k,
+                             &bars->k_full[st], s * 64, j * kBlockN, u.bh, keep);
+          mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
+#pragma unroll
+          for (int s = 0; s < C::kSub; ++s)
+            tma_load_3d_hint(smem + C::kVOff + st * C::kTileBytes + s * C::kSubBytes, &tm_v,
+                             &bars->v_full[st], s * 64, j * kBlockN, u.bh, keep);
+        }
+        __syncwarp();
+      }
     }
     // Drain: every copy issued must have landed before this CTA may exit.
-    const WaitCtl drain{&bars->never, nullptr, p.timeout_ns};
-    if (load_q) mbar_wait_warp(&bars->q_full, 0, drain);
-    const int issued = j;
-    for (int st = 0; st < C::kStages && st < issued; ++st) {
-      const int last_use = (issued - 1 - st) / C::kStages;
+    if (load_q) {
+      for (int b = 0; b < C::kQBufs && b < qn; ++b) {
+        const int last = (qn - 1 - b) / C::kQBufs;  // last use of buffer b
+        mbar_wait_warp(&bars->q_full[b], last & 1, drain);
+      }
+    }
+    for (int st = 0; st < C::kStages && st < g; ++st) {
+      const int last_use = (g - 1 - st) / C::kStages;
       mbar_wait_warp(&bars->k_full[st], last_use & 1, drain);
       mbar_wait_warp(&bars->v_full[st], last_use & 1, drain);
     }
@@ -212,7 +256,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp runs the schedule and waits (uniform control flow); lane 0 alone
     // issues each batch of tcgen05.mma and the commit that tracks it.
     const bool leader = lane == 0;
-    const WaitCtl drain{&bars->never, nullptr, p.timeout_ns};
     auto commit = [&](uint64_t* bar) {
       if (leader) mma_commit(bar);
       __syncwarp();
@@ -223,9 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescS = idesc_bf16(kBlockM, kBlockN, false);
       const uint32_t q_base = smem_u32(smem + C::kQOff);
       const uint32_t k_base = smem_u32(smem + C::kKOff);
-      auto issue_s = [&](int i, int st) {
+      auto issue_s = [&](int qb, int i, int st) {
         if (leader) {
-          const uint32_t qa = q_base + i * C::kTileBytes;
+          const uint32_t qa = q_base + (qb * 2 + i) * C::kTileBytes;
           const uint32_t ka = k_base + st * C::kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -237,26 +280,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       };
-      bool ok = n_steps > 0 && mbar_wait_warp(&bars->q_full, 0, wc);
-      for (int j = 0; ok && j < n_steps; ++j) {
-        const int st = j % C::kStages;
-        if (!mbar_wait_warp(&bars->k_full[st], (j / C::kStages) & 1, wc)) { ok = false; break; }
-        tc_fence_after_sync();
+      int g = 0, qn = 0;
+      int ns[2] = {0, 0};   // S_i issued so far
+      bool ok = true;
+      for (int r = 0; ok && r * grid < p.total_units; ++r) {
+        const int L = unit_index(r, cta, grid);
+        if (L >= p.total_units) continue;
+        const Unit u = unit_of<CAUSAL>(p, L);
+        const int qb = qn % C::kQBufs;
+        if (!mbar_wait_warp(&bars->q_full[qb], (qn / C::kQBufs) & 1, wc)) { ok = false; break; }
+        for (int j = 0; j < u.n_steps; ++j, ++g) {
+          const int st = g % C::kStages;
+          if (!mbar_wait_warp(&bars->k_full[st], (g / C::kStages) & 1, wc)) { ok = false; break; }
+          tc_fence_after_sync();
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (j >= nkv[i]) continue;
-          if (j > 0) {
-            // S_i may be overwritten once its softmax has read it (P in its own columns)
-            // or, when P_i lives in S_i's columns, once P_i·V has consumed P_i.
-            uint64_t* freed = C::kSepP ? &bars->s_free[i] : &bars->pv_done[i];
-            if (!mbar_wait_warp(freed, (j - 1) & 1, wc)) { ok = false; break; }
-            tc_fence_after_sync();
+          for (int i = 0; i < 2; ++i) {
+            if (j >= u.nkv[i]) continue;
+            if (ns[i] > 0) {
+              // S_i may be overwritten once its softmax has read it (P in its own columns)
+              // or, when P_i lives in S_i's columns, once P_i·V has consumed P_i.
+              uint64_t* freed = C::kSepP ? &bars->s_free[i] : &bars->pv_done[i];
+              if (!mbar_wait_warp(freed, (ns[i] - 1) & 1, wc)) { ok = false; break; }
+              tc_fence_after_sync();
+            }
+            issue_s(qb, i, st);
+            ++ns[i];
+            FA_TRACE(16 + i, j);
           }
-          issue_s(i, st);
-          FA_TRACE(16 + i, j);
+          if (!ok) break;
+          commit(&bars->kv_empty[st]);  // K_j is free once these S MMAs are done
         }
         if (!ok) break;
-        commit(&bars->kv_empty[st]);  // K_j is free once these S MMAs are done
+        commit(&bars->q_empty[qb]);     // this unit's Q is free once its S MMAs are done
+        ++qn;
       }
     } else {
       // O_i += P_i · V_st : A = P from TMEM (8 columns = 16 keys per step), B = V tile,
@@ -278,21 +334,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       };
-      bool ok = n_steps > 0;
-      for (int j = 0; ok && j < n_steps; ++j) {
-        const int st = j % C::kStages;
-        if (!mbar_wait_warp(&bars->v_full[st], (j / C::kStages) & 1, wc)) { ok = false; break; }
+      int g = 0;
+      int np[2] = {0, 0};       // P_i·V issued so far
+      int nunits[2] = {0, 0};   // finished units in which tile i was active
+      bool ok = true;
+      for (int r = 0; ok && r * grid < p.total_units; ++r) {
+        const int L = unit_index(r, cta, grid);
+        if (L >= p.total_units) continue;
+        const Unit u = unit_of<CAUSAL>(p, L);
+        for (int j = 0; j < u.n_steps; ++j, ++g) {
+          const int st = g % C::kStages;
+          if (!mbar_wait_warp(&bars->v_full[st], (g / C::kStages) & 1, wc)) { ok = false; break; }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          if (j >= nkv[i]) continue;
-          if (!mbar_wait_warp(&bars->p_full[i], j & 1, wc)) { ok = false; break; }
-          FA_TRACE(11 + i, j);
-          tc_fence_after_sync();
-          issue_pv(i, st, j > 0);
-          FA_TRACE(14 + i, j);
+          for (int i = 0; i < 2; ++i) {
+            if (j >= u.nkv[i]) continue;
+            if (j == 0 && nunits[i] > 0) {
+              // This unit's first P·V overwrites O_i: the previous unit's O_i must have
+              // been read out.
+              if (!mbar_wait_warp(&bars->o_free[i], (nunits[i] - 1) & 1, wc)) { ok = false; break; }
+            }
+            if (!mbar_wait_warp(&bars->p_full[i], np[i] & 1, wc)) { ok = false; break; }
+            FA_TRACE(11 + i, j);
+            tc_fence_after_sync();
+            issue_pv(i, st, j > 0);
+            ++np[i];
+            FA_TRACE(14 + i, j);
+          }
+          if (!ok) break;
+          commit(&bars->kv_empty[st]);  // V_j is free once these P·V MMAs are done
         }
-        if (!ok) break;
-        commit(&bars->kv_empty[st]);  // V_j is free once these P·V MMAs are done
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+          if (u.nkv[i] > 0) ++nunits[i];
       }
     }
     // Nothing may still be running on the tensor core when TMEM is released.
@@ -303,142 +376,159 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = warp >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const int qt = qt0 + wg;
-    const int q_row = qt * kBlockM + row;
-    const int n = nkv[wg];
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t t_s = tmem + lane_off + C::col_s(wg);
     const uint32_t t_o = tmem + lane_off + C::col_o(wg);
     const uint32_t t_p = tmem + lane_off + C::col_p(wg);
     const float c = p.scale_log2;
+    const uint32_t nan2 = 0x7FC07FC0u;  // two bf16 quiet NaNs
 
-    float m_ref = -INFINITY;  // reference max (base-2 scaled units) shared by O and l
-    float l = 0.0f;
+    int gs = 0;     // S_i consumed (= P_i produced) so far over this CTA's units
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      if (!mbar_wait_warp(&bars->s_full[wg], j & 1, wc)) { ok = false; break; }
-      FA_TRACE(30 + wg, j);
-      tc_fence_after_sync();
-      const int k0 = j * kBlockN;
-      const bool masked = (CAUSAL && j == qt) || (k0 + kBlockN > p.T);
-      // Keys past the end of the sequence, and (diagonal tile) keys after this query.
-      const int lim = (CAUSAL ? min(q_row + 1, p.T) : p.T) - k0;
-
-      // S in two halves: the second half loads while the first is masked and maxed.
-      uint32_t s[kBlockN];
-      tmem_ld32(t_s + 0, s);
-      tmem_ld32(t_s + 32, s + 32);
-      tmem_ld_wait();
-      reg_fence32(s);
-      reg_fence32(s + 32);
-      tmem_ld32(t_s + 64, s + 64);
-      tmem_ld32(t_s + 96, s + 96);
-      if (masked) {
-#pragma unroll
-        for (int t = 0; t < 64; ++t)
-          if (t >= lim) s[t] = __float_as_uint(-INFINITY);
-      }
-      float mx[8];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) mx[a] = fmaxf(u2f(s[2 * a]), u2f(s[2 * a + 1]));
-#pragma unroll
-      for (int t = 16; t < 64; t += 16)
-#pragma unroll
-        for (int a = 0; a < 8; ++a) mx[a] = fmax3(mx[a], u2f(s[t + 2 * a]), u2f(s[t + 2 * a + 1]));
-      tmem_ld_wait();
-      reg_fence32(s + 64);
-      reg_fence32(s + 96);
-      if constexpr (C::kSepP) {
-        // S_i is in registers: the tensor core may overwrite it with the next S_i.
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_free[wg]);
-      }
-      FA_TRACE(20 + wg, j);
-      if (masked) {
-#pragma unroll
-        for (int t = 64; t < kBlockN; ++t)
-          if (t >= lim) s[t] = __float_as_uint(-INFINITY);
-      }
-#pragma unroll
-      for (int t = 64; t < kBlockN; t += 16)
-#pragma unroll
-        for (int a = 0; a < 8; ++a) mx[a] = fmax3(mx[a], u2f(s[t + 2 * a]), u2f(s[t + 2 * a + 1]));
-      const float m_tile =
-          fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c;
-      FA_TRACE(40 + wg, j);
-
-      float alpha = 1.0f;
-      bool rescale = false;
-      if (j == 0) {
-        m_ref = m_tile;
-      } else if (m_tile > m_ref + kTau) {
-        alpha = ex2_approx(m_ref - m_tile);
-        m_ref = m_tile;
-        l *= alpha;
-        rescale = true;
-      }
-
-      // p = 2^(s·c − m_ref) on fp32 pairs; row sum in fp32; P kept as bf16 pairs.
-      const uint64_t c2 = f2_pack(c, c);
-      const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
-      uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-      uint32_t pk[kBlockN / 2];
-#pragma unroll
-      for (int t = 0; t < kBlockN / 2; ++t) {
-        const uint64_t x2 = f2_fma(f2_pack(u2f(s[2 * t]), u2f(s[2 * t + 1])), c2, nm2);
-        float x0, x1;
-        f2_unpack(x2, x0, x1);
-        const float p0 = ex2_approx(x0);
-        const float p1 = ex2_approx(x1);
-        if (t & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
-        else acc0 = f2_add(acc0, f2_pack(p0, p1));
-        pk[t] = pack_bf16x2(p0, p1);
-      }
-      {
-        float a0, a1, b0, b1;
-        f2_unpack(acc0, a0, a1);
-        f2_unpack(acc1, b0, b1);
-        l += (a0 + b0) + (a1 + b1);
-      }
-      FA_TRACE(42 + wg, j);
-      if constexpr (C::kSepP) {
-        // P_i's columns and O_i are free once the previous P_i·V has finished.
-        if (j > 0) {
-          if (!mbar_wait_warp(&bars->pv_done[wg], (j - 1) & 1, wc)) { ok = false; break; }
-          tc_fence_after_sync();
-        }
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-        // Rows whose max jumped bring their accumulated O to the new reference. O is
-        // stable here (the previous P·V is done) and not read again before p_full.
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(t_o + c0, r);
-          tmem_ld_wait();
-          reg_fence32(r);
-#pragma unroll
-          for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(u2f(r[t]) * alpha);
-          tmem_st32(t_o + c0, r);
-        }
-      }
-      tmem_st32(t_p + 0, pk);
-      tmem_st32(t_p + 32, pk + 32);
-      tmem_st_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[wg]);
-      FA_TRACE(22 + wg, j);
-    }
-
-    if (n > 0) {
-      const bool good = ok && mbar_wait_warp(&bars->pv_done[wg], (n - 1) & 1, wc);
-      FA_TRACE(24 + wg, 0);
-      const size_t row_idx = static_cast<size_t>(bh) * static_cast<size_t>(p.T) +
+    for (int r = 0; r * grid < p.total_units; ++r) {
+      const int L = unit_index(r, cta, grid);
+      if (L >= p.total_units) continue;
+      const Unit u = unit_of<CAUSAL>(p, L);
+      const int n = u.nkv[wg];
+      if (n == 0) continue;
+      const int qt = u.qt0 + wg;
+      const int q_row = qt * kBlockM + row;
+      const size_t row_idx = static_cast<size_t>(u.bh) * static_cast<size_t>(p.T) +
                              static_cast<size_t>(q_row);
       const bool in_range = q_row < p.T;
       uint4* orow = reinterpret_cast<uint4*>(p.o + row_idx * D);
+      if (!ok) {
+        // A wait gave up earlier: mark every row this warpgroup owns as failed.
+        if (in_range) {
+#pragma unroll
+          for (int t = 0; t < D / 8; ++t) orow[t] = make_uint4(nan2, nan2, nan2, nan2);
+          p.lse[row_idx] = __uint_as_float(0x7FC00000u);
+        }
+        continue;
+      }
+
+      float m_ref = -INFINITY;  // reference max (base-2 scaled units) shared by O and l
+      float l = 0.0f;
+      for (int j = 0; j < n; ++j, ++gs) {
+        if (!mbar_wait_warp(&bars->s_full[wg], gs & 1, wc)) { ok = false; break; }
+        FA_TRACE(30 + wg, j);
+        tc_fence_after_sync();
+        const int k0 = j * kBlockN;
+        const bool masked = (CAUSAL && j == qt) || (k0 + kBlockN > p.T);
+        // Keys past the end of the sequence, and (diagonal tile) keys after this query.
+        const int lim = (CAUSAL ? min(q_row + 1, p.T) : p.T) - k0;
+
+        // S in two halves: the second half loads while the first is masked and maxed.
+        uint32_t s[kBlockN];
+        tmem_ld32(t_s + 0, s);
+        tmem_ld32(t_s + 32, s + 32);
+        tmem_ld_wait();
+        reg_fence32(s);
+        reg_fence32(s + 32);
+        tmem_ld32(t_s + 64, s + 64);
+        tmem_ld32(t_s + 96, s + 96);
+        if (masked) {
+#pragma unroll
+          for (int t = 0; t < 64; ++t)
+            if (t >= lim) s[t] = __float_as_uint(-INFINITY);
+        }
+        float mx[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx[a] = fmaxf(u2f(s[2 * a]), u2f(s[2 * a + 1]));
+#pragma unroll
+        for (int t = 16; t < 64; t += 16)
+#pragma unroll
+          for (int a = 0; a < 8; ++a) mx[a] = fmax3(mx[a], u2f(s[t + 2 * a]), u2f(s[t + 2 * a + 1]));
+        tmem_ld_wait();
+        reg_fence32(s + 64);
+        reg_fence32(s + 96);
+        if constexpr (C::kSepP) {
+          // S_i is in registers: the tensor core may overwrite it with the next S_i.
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->s_free[wg]);
+        }
+        FA_TRACE(20 + wg, j);
+        if (masked) {
+#pragma unroll
+          for (int t = 64; t < kBlockN; ++t)
+            if (t >= lim) s[t] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int t = 64; t < kBlockN; t += 16)
+#pragma unroll
+          for (int a = 0; a < 8; ++a) mx[a] = fmax3(mx[a], u2f(s[t + 2 * a]), u2f(s[t + 2 * a + 1]));
+        const float m_tile =
+            fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c;
+        FA_TRACE(40 + wg, j);
+
+        float alpha = 1.0f;
+        bool rescale = false;
+        if (j == 0) {
+          m_ref = m_tile;
+        } else if (m_tile > m_ref + kTau) {
+          alpha = ex2_approx(m_ref - m_tile);
+          m_ref = m_tile;
+          l *= alpha;
+          rescale = true;
+        }
+
+        // p = 2^(s·c − m_ref) on fp32 pairs; row sum in fp32; P kept as bf16 pairs.
+        const uint64_t c2 = f2_pack(c, c);
+        const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
+        uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+        uint32_t pk[kBlockN / 2];
+#pragma unroll
+        for (int t = 0; t < kBlockN / 2; ++t) {
+          const uint64_t x2 = f2_fma(f2_pack(u2f(s[2 * t]), u2f(s[2 * t + 1])), c2, nm2);
+          float x0, x1;
+          f2_unpack(x2, x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          if (t & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
+          else acc0 = f2_add(acc0, f2_pack(p0, p1));
+          pk[t] = pack_bf16x2(p0, p1);
+        }
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(acc0, a0, a1);
+          f2_unpack(acc1, b0, b1);
+          l += (a0 + b0) + (a1 + b1);
+        }
+        FA_TRACE(42 + wg, j);
+        if constexpr (C::kSepP) {
+          // P_i's columns and O_i are free once the previous P_i·V has finished.
+          if (gs > 0) {
+            if (!mbar_wait_warp(&bars->pv_done[wg], (gs - 1) & 1, wc)) { ok = false; break; }
+            tc_fence_after_sync();
+          }
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+          // Rows whose max jumped bring their accumulated O to the new reference. O is
+          // stable here (the previous P·V is done) and not read again before p_full.
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(t_o + c0, r);
+            tmem_ld_wait();
+            reg_fence32(r);
+#pragma unroll
+            for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(u2f(r[t]) * alpha);
+            tmem_st32(t_o + c0, r);
+          }
+        }
+        tmem_st32(t_p + 0, pk);
+        tmem_st32(t_p + 32, pk + 32);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full[wg]);
+        FA_TRACE(22 + wg, j);
+      }
+
+      // Epilogue: O / l and the logsumexp, once this unit's last P·V is done.
+      const bool good = ok && mbar_wait_warp(&bars->pv_done[wg], (gs - 1) & 1, wc);
+      FA_TRACE(24 + wg, 0);
       if (good) {
         tc_fence_after_sync();
         const float inv_l = 1.0f / l;
@@ -458,13 +548,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               orow[c0 / 8 + t] = make_uint4(ob[4 * t], ob[4 * t + 1], ob[4 * t + 2], ob[4 * t + 3]);
           }
         }
+        // O_i has been read: the next unit's first P·V may overwrite it.
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_free[wg]);
         if (in_range) p.lse[row_idx] = (m_ref + log2f(l)) * 0.69314718055994530942f;
         FA_TRACE(26 + wg, 0);
-      } else if (in_range) {
-        const uint32_t nan2 = 0x7FC07FC0u;  // two bf16 quiet NaNs
+      } else {
+        ok = false;
+        if (in_range) {
 #pragma unroll
-        for (int t = 0; t < D / 8; ++t) orow[t] = make_uint4(nan2, nan2, nan2, nan2);
-        p.lse[row_idx] = __uint_as_float(0x7FC00000u);
+          for (int t = 0; t < D / 8; ++t) orow[t] = make_uint4(nan2, nan2, nan2, nan2);
+          p.lse[row_idx] = __uint_as_float(0x7FC00000u);
+        }
       }
     }
   }
