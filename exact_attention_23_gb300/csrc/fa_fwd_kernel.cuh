@@ -103,6 +103,7 @@ struct FwdParams {
   int total_units;    // n_units · BH
   int n_kv;           // ceil(T/128): K/V tiles, also Q tiles
   int tiles_per_cta;  // 2 (ping-pong pair) or 1 (short sequences: more CTAs)
+  int head_group;     // heads whose units are interleaved (their K/V fit in L2 together)
   float scale_log2;   // scale · log2(e)
   uint64_t timeout_ns;
   uint32_t flags;
@@ -110,11 +111,12 @@ struct FwdParams {
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
-// One work unit. Units are numbered heaviest first (under the causal mask the cost of a
-// Q-tile pair grows with its position), all heads of one position together; CTA c takes
-// the units of round r = 0, 1, 2, ... at position c in even rounds and G−1−c in odd rounds
-// (G = grid size). Over a list sorted by cost this zig-zag gives every CTA nearly the same
-// total work without any shared counter.
+// One work unit. Heads are taken in groups small enough for their K/V to stay in L2
+// together; within a group, units are numbered heaviest first (under the causal mask the
+// cost of a Q-tile pair grows with its position), all heads of the group at one position
+// together. CTA c takes the units of round r = 0, 1, 2, ... at position c in even rounds
+// and G−1−c in odd rounds (G = grid size). Over a list sorted by cost this zig-zag gives
+// every CTA nearly the same total work without any shared counter.
 struct Unit {
   int bh, qt0, nkv[2], n_steps;
 };
@@ -126,8 +128,12 @@ __device__ __forceinline__ int unit_index(int round, int cta, int grid) {
 template <bool CAUSAL>
 __device__ __forceinline__ Unit unit_of(const FwdParams& p, int L) {
   Unit u;
-  u.bh = L % p.BH;
-  const int idx = p.n_units - 1 - L / p.BH;
+  const int per_group = p.n_units * p.head_group;
+  const int grp = L / per_group;
+  const int within = L - grp * per_group;
+  const int gsize = min(p.head_group, p.BH - grp * p.head_group);
+  u.bh = grp * p.head_group + within % gsize;
+  const int idx = p.n_units - 1 - within / gsize;
   u.qt0 = idx * p.tiles_per_cta;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
