@@ -1,4 +1,4 @@
-"""Plain, slow fp64 oracle for scaled-dot-product attention (forward only).
+"""Plain, slow fp64 oracle for scaled-dot-product attention (forward and backward).
 
 TEST INFRASTRUCTURE ONLY: never imported by the product path.
 
@@ -30,8 +30,20 @@ by exp(m_old − m_new), accumulator rescaled by the same factor, one final ÷l)
 separately by :func:`online_softmax_trace` and :func:`online_weighted_sum`, so that the
 tests can pin the recurrence itself against the one-pass definition.
 
-Pinned by ``tests/test_oracle.py`` (closed forms, invariants, brute force and
-planted-mistake checks); nothing here is "parity unpinned".
+The backward pass (:func:`attention_backward`) is the derivative of that same definition
+with respect to Q, K and V for an upstream gradient dO, written out by the chain rule:
+
+    dV = Pᵀ·dO,   dP = dO·Vᵀ,   dS_ij = P_ij·(dP_ij − Σ_k P_ik·dP_ik),
+    dQ = scale·dS·K,   dK = scale·dSᵀ·Q.
+
+[HW-FA] step ④ ("can this kernel train?") says the forward keeps only the per-row
+logsumexp so that the backward can recompute S and P block by block, and [FA-tiling]
+§2.2 (FlashAttention core ideas, ijyty.com: backward recomputation, per-block gradients
+summed into the global gradient). Neither page prints a backward formula, so this is the
+plain derivative, evaluated naively on the whole score row.
+
+Pinned by ``tests/test_oracle.py`` (closed forms, invariants, brute force, finite
+differences and planted-mistake checks); nothing here is "parity unpinned".
 """
 
 from __future__ import annotations
@@ -182,3 +194,114 @@ def online_weighted_sum(x, vals, block: int):
         acc = acc * alpha + p @ vals[start:start + block]
         m = m_new
     return acc / l, m, l
+
+
+# --------------------------------------------------------------------------------------
+# Backward pass: the derivative of the forward definition.
+# --------------------------------------------------------------------------------------
+
+def grad_values(p: np.ndarray, do_rows: np.ndarray) -> np.ndarray:
+    """dV contribution of these query rows: Pᵀ·dO (O = P·V is linear in V)."""
+    return p.T @ do_rows
+
+
+def grad_probs(do_rows: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """dP = dO·Vᵀ."""
+    return do_rows @ v.T
+
+
+def softmax_backward(p: np.ndarray, dp: np.ndarray) -> np.ndarray:
+    """dS = P ∘ (dP − rowsum(P ∘ dP)): the Jacobian of a softmax row applied to dP
+    (masked entries have P = 0 and get dS = 0)."""
+    return p * (dp - np.sum(p * dp, axis=1, keepdims=True))
+
+
+def grad_queries(ds: np.ndarray, k: np.ndarray, scale: float) -> np.ndarray:
+    """dQ rows = scale·dS·K (S = scale·Q·Kᵀ)."""
+    return scale * (ds @ k)
+
+
+def grad_keys(ds: np.ndarray, q_rows: np.ndarray, scale: float) -> np.ndarray:
+    """dK contribution of these query rows: scale·dSᵀ·Q."""
+    return scale * (ds.T @ q_rows)
+
+
+def attention_backward_head(q, k, v, do, causal: bool, scale: float, row_chunk: int = 512):
+    """(dQ, dK, dV) of one (batch, head); q, k, v, do: [T, d]. Query rows are taken in
+    chunks; each chunk's terms are exact and dK, dV are sums over query rows."""
+    q = _as_f64(q)
+    k = _as_f64(k)
+    v = _as_f64(v)
+    do = _as_f64(do)
+    T = q.shape[0]
+    dq = np.empty_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for r0 in range(0, T, row_chunk):
+        rows = np.arange(r0, min(T, r0 + row_chunk))
+        s = scores(q[rows], k, scale)
+        if causal:
+            s = apply_causal_mask(s, rows)
+        p, _, _ = safe_softmax(s)
+        dv += grad_values(p, do[rows])
+        ds = softmax_backward(p, grad_probs(do[rows], v))
+        dq[rows] = grad_queries(ds, k, scale)
+        dk += grad_keys(ds, q[rows], scale)
+    return dq, dk, dv
+
+
+def attention_backward_rows(q, k, v, do, causal: bool, scale: float, rows):
+    """dQ of the given query rows only (one head; [T, d] inputs). Each dQ row needs only
+    its own row of P and dP, so sampled rows can be checked at any T."""
+    q = _as_f64(q)
+    k = _as_f64(k)
+    v = _as_f64(v)
+    do = _as_f64(do)
+    rows = np.asarray(rows)
+    s = scores(q[rows], k, scale)
+    if causal:
+        s = apply_causal_mask(s, rows)
+    p, _, _ = safe_softmax(s)
+    ds = softmax_backward(p, grad_probs(do[rows], v))
+    return grad_queries(ds, k, scale)
+
+
+def attention_backward_cols(q, k, v, do, causal: bool, scale: float, cols,
+                            row_chunk: int = 512):
+    """dK and dV of the given key rows only (one head): each needs one column of P and dS
+    over all query rows, taken here in chunks of query rows."""
+    q = _as_f64(q)
+    k = _as_f64(k)
+    v = _as_f64(v)
+    do = _as_f64(do)
+    cols = np.asarray(cols)
+    T = q.shape[0]
+    dk = np.zeros((len(cols), k.shape[1]))
+    dv = np.zeros((len(cols), v.shape[1]))
+    for r0 in range(0, T, row_chunk):
+        rows = np.arange(r0, min(T, r0 + row_chunk))
+        s = scores(q[rows], k, scale)
+        if causal:
+            s = apply_causal_mask(s, rows)
+        p, _, _ = safe_softmax(s)
+        ds = softmax_backward(p, grad_probs(do[rows], v))
+        dv += grad_values(p[:, cols], do[rows])
+        dk += grad_keys(ds[:, cols], q[rows], scale)
+    return dk, dv
+
+
+def attention_backward(q, k, v, do, causal: bool, scale: float):
+    """Gradients of L = Σ dO ∘ O with respect to q, k, v ([B, H, T, d] arrays, fp64 out)."""
+    q = _as_f64(q)
+    k = _as_f64(k)
+    v = _as_f64(v)
+    do = _as_f64(do)
+    B, H, T, d = q.shape
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    for b in range(B):
+        for h in range(H):
+            dq[b, h], dk[b, h], dv[b, h] = attention_backward_head(
+                q[b, h], k[b, h], v[b, h], do[b, h], causal, scale)
+    return dq, dk, dv

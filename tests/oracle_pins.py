@@ -260,10 +260,129 @@ def pin_sdpa_library(orc):
         assert np.max(np.abs(o - ot)) <= 1e-12
 
 
+# ------------------------------------------------------------------ backward-pass pins
+
+def _loss_bruteforce(q, k, v, do, causal, scale):
+    """L = Σ dO ∘ O with O from the pure-Python definition."""
+    o, _ = brute_force(q, k, v, causal, scale)
+    return float(np.sum(np.asarray(do) * o))
+
+
+def pin_bwd_finite_diff(orc):
+    """Every gradient element equals a central difference of L = Σ dO ∘ O, with the
+    forward taken from the pure-Python loops (not from the oracle), within 1e-7."""
+    cases = [(1, 1, 5, 3, True), (1, 1, 5, 3, False), (1, 2, 4, 2, True)]
+    h = 1e-5
+    for n, (B, H, T, d, causal) in enumerate(cases):
+        q, k, v = _qkv(200 + n, B, H, T, d)
+        do = _rng(300 + n).standard_normal((B, H, T, d))
+        scale = 0.7
+        grads = orc.attention_backward(q, k, v, do, causal, scale)
+        for which, g in enumerate(grads):
+            base = [q, k, v]
+            for idx in np.ndindex(*q.shape):
+                plus = [t.copy() for t in base]
+                minus = [t.copy() for t in base]
+                plus[which][idx] += h
+                minus[which][idx] -= h
+                fd = (_loss_bruteforce(*plus, do, causal, scale)
+                      - _loss_bruteforce(*minus, do, causal, scale)) / (2 * h)
+                assert abs(g[idx] - fd) <= 1e-7, (n, which, idx, g[idx], fd)
+
+
+def pin_bwd_hand_example(orc):
+    """T=2, d=1, no mask, worked by hand. With p_i = σ(c·a_i·(k1 − k0)) the weight of key 1
+    in row i, O_i = v0 + p_i·(v1 − v0), so for L = Σ g_i·O_i:
+    dL/da_i = g_i·(v1 − v0)·p_i(1 − p_i)·c·(k1 − k0); dL/dv1 = Σ g_i·p_i;
+    dL/dv0 = Σ g_i·(1 − p_i); dL/dk1 = Σ g_i·(v1 − v0)·p_i(1 − p_i)·c·a_i = −dL/dk0."""
+    a = np.array([0.8, -1.3])
+    kk = np.array([0.4, 1.1])
+    vv = np.array([2.0, -0.5])
+    g = np.array([1.5, 0.25])
+    c = 0.9
+    q = a.reshape(1, 1, 2, 1)
+    k = kk.reshape(1, 1, 2, 1)
+    v = vv.reshape(1, 1, 2, 1)
+    do = g.reshape(1, 1, 2, 1)
+    dq, dk, dv = orc.attention_backward(q, k, v, do, False, c)
+    p = 1.0 / (1.0 + np.exp(-c * a * (kk[1] - kk[0])))
+    w = g * (vv[1] - vv[0]) * p * (1 - p) * c
+    assert np.max(np.abs(dq[0, 0, :, 0] - w * (kk[1] - kk[0]))) <= 1e-14
+    assert abs(dv[0, 0, 1, 0] - np.sum(g * p)) <= 1e-14
+    assert abs(dv[0, 0, 0, 0] - np.sum(g * (1 - p))) <= 1e-14
+    assert abs(dk[0, 0, 1, 0] - np.sum(w * a)) <= 1e-14
+    assert abs(dk[0, 0, 0, 0] + np.sum(w * a)) <= 1e-14
+    # causal: row 0 sees only key 0 (O_0 = v0); row 1 as above
+    dq, dk, dv = orc.attention_backward(q, k, v, do, True, c)
+    assert dq[0, 0, 0, 0] == 0.0
+    assert abs(dq[0, 0, 1, 0] - w[1] * (kk[1] - kk[0])) <= 1e-14
+    assert abs(dv[0, 0, 0, 0] - (g[0] + g[1] * (1 - p[1]))) <= 1e-14
+    assert abs(dv[0, 0, 1, 0] - g[1] * p[1]) <= 1e-14
+    assert abs(dk[0, 0, 1, 0] - w[1] * a[1]) <= 1e-14
+
+
+def pin_bwd_invariants(orc):
+    """Shifting every key by u leaves O unchanged, so Σ_j dK_j = 0; adding c to every
+    value row adds c to every output row, so Σ_j dV_j = Σ_i dO_i; with V constant O does
+    not depend on Q or K, so dQ = dK = 0; causal query 0 sees one key, so dQ_0 = 0, and
+    the last key is seen by the last query alone: dV_{T−1} = P_{T−1,T−1}·dO_{T−1}."""
+    B, H, T, d = 2, 2, 33, 5
+    q, k, v = _qkv(21, B, H, T, d, std=1.3)
+    do = _rng(22).standard_normal((B, H, T, d))
+    scale = 0.45
+    for causal in (False, True):
+        dq, dk, dv = orc.attention_backward(q, k, v, do, causal, scale)
+        assert np.max(np.abs(dk.sum(axis=2))) <= 1e-12
+        assert np.max(np.abs(dv.sum(axis=2) - do.sum(axis=2))) <= 1e-12
+        vc = np.broadcast_to(np.linspace(-1.0, 2.0, d), v.shape).copy()
+        dq0, dk0, _ = orc.attention_backward(q, k, vc, do, causal, scale)
+        assert np.max(np.abs(dq0)) <= 1e-12 and np.max(np.abs(dk0)) <= 1e-12
+        if causal:
+            assert np.max(np.abs(dq[:, :, 0])) == 0.0
+            o, lse = orc.attention(q, k, v, True, scale)
+            s_last = scale * np.einsum("bhd,bhd->bh", q[:, :, -1], k[:, :, -1])
+            p_last = np.exp(s_last - lse[:, :, -1])
+            assert np.max(np.abs(dv[:, :, -1] - p_last[..., None] * do[:, :, -1])) <= 1e-13
+
+
+def pin_bwd_autograd(orc):
+    """Cross-check against PyTorch autograd through its CPU scaled_dot_product_attention
+    in fp64 (a library routine for the same derivative)."""
+    import torch
+    import torch.nn.functional as F
+    q, k, v = _qkv(23, 2, 2, 41, 16)
+    do = _rng(24).standard_normal(q.shape)
+    for causal in (False, True):
+        tq, tk, tv = (torch.from_numpy(t.copy()).requires_grad_(True) for t in (q, k, v))
+        out = F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=0.25)
+        out.backward(torch.from_numpy(do))
+        got = orc.attention_backward(q, k, v, do, causal, 0.25)
+        for g, t in zip(got, (tq, tk, tv)):
+            assert np.max(np.abs(g - t.grad.numpy())) <= 1e-12
+
+
+def pin_bwd_sampled(orc):
+    """dQ of sampled query rows and dK, dV of sampled key rows equal the full gradient on
+    those rows (several row chunks, a ragged last chunk)."""
+    q, k, v = _qkv(25, 1, 1, 1100, 8)
+    do = _rng(26).standard_normal(q.shape)
+    rows = np.array([0, 1, 511, 512, 513, 1023, 1099])
+    for causal in (False, True):
+        dq, dk, dv = orc.attention_backward(q, k, v, do, causal, 0.3)
+        dqr = orc.attention_backward_rows(q[0, 0], k[0, 0], v[0, 0], do[0, 0], causal, 0.3, rows)
+        dkc, dvc = orc.attention_backward_cols(q[0, 0], k[0, 0], v[0, 0], do[0, 0], causal, 0.3,
+                                               rows)
+        assert np.max(np.abs(dqr - dq[0, 0, rows])) <= 1e-12
+        assert np.max(np.abs(dkc - dk[0, 0, rows])) <= 1e-12
+        assert np.max(np.abs(dvc - dv[0, 0, rows])) <= 1e-12
+
+
 ORACLE_PINS = [pin_bruteforce, pin_hand_example, pin_row_sums, pin_constant_v,
                pin_causal_row0, pin_uniform, pin_shift, pin_permutation, pin_large_scores,
                pin_rows_match_full, pin_sdpa_library]
 RECURRENCE_PINS = [pin_online_trace, pin_online_weighted_sum]
+BACKWARD_PINS = [pin_bwd_finite_diff, pin_bwd_hand_example, pin_bwd_invariants,
+                 pin_bwd_autograd, pin_bwd_sampled]
 
 
 def load_page_facts():
@@ -283,4 +402,4 @@ def run_all(orc, pins):
     return failed
 
 
-__all__ = ["ORACLE_PINS", "RECURRENCE_PINS", "run_all", "brute_force", "load_page_facts"]
+__all__ = ["ORACLE_PINS", "RECURRENCE_PINS", "BACKWARD_PINS", "run_all", "brute_force", "load_page_facts"]

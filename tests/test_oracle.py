@@ -11,8 +11,10 @@ import oracle.naive as oa
 from tests import oracle_pins as pins
 
 
-@pytest.mark.parametrize("pin", pins.ORACLE_PINS + pins.RECURRENCE_PINS,
-                         ids=lambda p: p.__name__)
+ALL_PINS = pins.ORACLE_PINS + pins.RECURRENCE_PINS + pins.BACKWARD_PINS
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
 def test_oracle_pin(pin):
     pin(oa)
 
@@ -29,7 +31,8 @@ def test_page_facts_are_consistent():
 
 
 def test_oracle_package_exports():
-    for name in ("attention", "attention_rows", "online_softmax_trace", "online_weighted_sum"):
+    for name in ("attention", "attention_rows", "online_softmax_trace", "online_weighted_sum",
+                 "attention_backward", "attention_backward_rows", "attention_backward_cols"):
         assert callable(getattr(oracle, name))
 
 
@@ -109,6 +112,34 @@ def _weighted_no_acc_rescale(x, vals, block):
     return acc / l, m, l
 
 
+def _dsoftmax_no_rowsum(p, dp):
+    return p * dp
+
+
+def _dsoftmax_rowsum_of_dp(p, dp):
+    return p * (dp - dp.sum(axis=1, keepdims=True))
+
+
+def _dsoftmax_sign(p, dp):
+    return p * (np.sum(p * dp, axis=1, keepdims=True) - dp)
+
+
+def _dq_no_scale(ds, k, scale):
+    return ds @ k
+
+
+def _dk_no_scale(ds, q_rows, scale):
+    return ds.T @ q_rows
+
+
+def _dp_wrong_operand(do_rows, v):
+    return do_rows @ (v[::-1]).T
+
+
+def _dv_unnormalised(p, do_rows):
+    return (p / p.max(axis=1, keepdims=True)).T @ do_rows
+
+
 MUTANTS = {
     "scores:no_scale": ("scores", _no_scale),
     "mask:wrong_direction": ("apply_causal_mask", _mask_wrong_way),
@@ -124,6 +155,16 @@ MUTANTS = {
     "weighted:no_acc_rescale": ("online_weighted_sum", _weighted_no_acc_rescale),
 }
 
+BACKWARD_MUTANTS = {
+    "dsoftmax:no_rowsum": ("softmax_backward", _dsoftmax_no_rowsum),
+    "dsoftmax:rowsum_of_dp": ("softmax_backward", _dsoftmax_rowsum_of_dp),
+    "dsoftmax:sign": ("softmax_backward", _dsoftmax_sign),
+    "dq:no_scale": ("grad_queries", _dq_no_scale),
+    "dk:no_scale": ("grad_keys", _dk_no_scale),
+    "dp:wrong_operand_order": ("grad_probs", _dp_wrong_operand),
+    "dv:unnormalised_p": ("grad_values", _dv_unnormalised),
+}
+
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_planted_mistake(name, monkeypatch):
@@ -133,5 +174,22 @@ def test_pins_catch_planted_mistake(name, monkeypatch):
     assert failed, f"no pin caught the planted mistake {name}"
 
 
+@pytest.mark.parametrize("name", sorted(BACKWARD_MUTANTS))
+def test_backward_pins_catch_planted_mistake(name, monkeypatch):
+    attr, broken = BACKWARD_MUTANTS[name]
+    monkeypatch.setattr(oa, attr, broken)
+    failed = pins.run_all(oa, pins.BACKWARD_PINS)
+    assert failed, f"no backward pin caught the planted mistake {name}"
+
+
+@pytest.mark.parametrize("name", ["scores:no_scale", "mask:drops_diagonal", "mask:none",
+                                  "softmax:unnormalised"])
+def test_backward_pins_catch_forward_mistake(name, monkeypatch):
+    """The backward pins also see a mistake in the shared forward steps."""
+    attr, broken = MUTANTS[name]
+    monkeypatch.setattr(oa, attr, broken)
+    assert pins.run_all(oa, pins.BACKWARD_PINS), name
+
+
 def test_unmodified_oracle_passes_every_pin():
-    assert pins.run_all(oa, pins.ORACLE_PINS + pins.RECURRENCE_PINS) == []
+    assert pins.run_all(oa, ALL_PINS) == []
