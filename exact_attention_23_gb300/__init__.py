@@ -1,10 +1,11 @@
-"""Exact attention forward for GB300 (sm_103a).
+"""Exact attention for GB300 (sm_103a).
 
 ``fwd(q, k, v, causal)`` returns ``(o, lse)`` for contiguous bf16 CUDA tensors of shape
 [B, H, T, d] (d = 64 or 128): o = softmax(scale·QKᵀ [+causal mask])·V in bf16 and the
-per-row natural-log logsumexp in fp32. The work is done by the CUDA kernels of
-``libfa.so`` through its C ABI (include/fa.h); this module only allocates the outputs
-with PyTorch and passes pointers and the current stream.
+per-row natural-log logsumexp in fp32. ``bwd(q, k, v, o, lse, do, causal)`` returns the
+gradients (dq, dk, dv) for d = 64. The work is done by the CUDA kernels of ``libfa.so``
+through its C ABI (include/fa.h); this module only allocates outputs and workspace with
+PyTorch and passes pointers and the current stream.
 """
 
 from __future__ import annotations
@@ -21,6 +22,9 @@ from ._binding import (  # noqa: F401
     FA_FLAG_TEST_STARVE_Q,
     FA_OK,
     FAError,
+    fa_bwd,
+    fa_bwd_ex,
+    fa_bwd_workspace_size,
     fa_fwd,
     fa_fwd_ex,
     lib,
@@ -72,6 +76,59 @@ def fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd")
     return out, lse
+
+
+def bwd_workspace(B: int, H: int, T: int, d: int, device=None):
+    """A uint8 CUDA tensor large enough to serve as fa_bwd's workspace (torch allocations
+    are 256-byte aligned)."""
+    import torch
+    n = fa_bwd_workspace_size(B, H, T, d)
+    if n == 0:
+        raise FAError(FA_ERR_INVALID_ARG, "fa_bwd_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def bwd(q, k, v, o, lse, do, causal: bool = True, scale: float | None = None, dq=None,
+        dk=None, dv=None, workspace=None, status=None, timeout_ns: int = 0, flags: int = 0):
+    """Attention backward through libfa.so on the current CUDA stream.
+
+    ``o`` and ``lse`` are the outputs of ``fwd`` for the same q, k, v, causal and scale;
+    ``do`` is the gradient of the loss with respect to o. Returns (dq, dk, dv).
+    ``workspace`` (see ``bwd_workspace``) may be passed to reuse it between calls.
+    """
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _check(t, n)
+    if not (q.shape == k.shape == v.shape == o.shape == do.shape):
+        raise ValueError("q, k, v, o and do must have the same shape")
+    B, H, T, d = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, T) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, T] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _check(t, n)
+    if workspace is None:
+        workspace = bwd_workspace(B, H, T, d, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    st_ptr = None if status is None else status.data_ptr()
+    with torch.cuda.device(q.device):
+        rc = fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                       B, H, T, d, causal, scale, st_ptr, timeout_ns, flags, stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_bwd")
+    return dq, dk, dv
+
+
+def bwd_flops(B: int, H: int, T: int, d: int, causal: bool) -> float:
+    """Algorithmic FLOPs of one backward: five T×T×d products (S, dP, dV, dK, dQ), i.e.
+    2.5 × the forward's count, halved when causal."""
+    return 2.5 * flops(B, H, T, d, causal)
 
 
 def flops(B: int, H: int, T: int, d: int, causal: bool) -> float:

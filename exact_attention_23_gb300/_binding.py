@@ -23,7 +23,8 @@ FA_ERR_TIMEOUT = 5
 FA_FLAG_TEST_STARVE_Q = 1
 
 # Every symbol include/fa.h declares.
-EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_strerror", "fa_version")
+EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_ex", "fa_strerror",
+           "fa_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -50,6 +51,14 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp,
                                     ctypes.c_ulonglong, ctypes.c_uint, vp]
             L.fa_fwd_ex.restype = i
+            sz = ctypes.c_size_t
+            L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+            L.fa_bwd_workspace_size.restype = sz
+            L.fa_bwd.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, vp]
+            L.fa_bwd.restype = i
+            L.fa_bwd_ex.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, vp, ctypes.c_ulonglong,
+                                                ctypes.c_uint, vp]
+            L.fa_bwd_ex.restype = i
             L.fa_strerror.argtypes = [i]
             L.fa_strerror.restype = ctypes.c_char_p
             L.fa_version.argtypes = []
@@ -75,3 +84,20 @@ def fa_fwd_ex(q, k, v, o, lse, B, H, T, d, causal, scale, status, timeout_ns, fl
               stream) -> int:
     return lib().fa_fwd_ex(q, k, v, o, lse, B, H, T, d, int(bool(causal)), float(scale),
                            status, int(timeout_ns), int(flags), stream)
+
+
+def fa_bwd_workspace_size(B, H, T, d) -> int:
+    return int(lib().fa_bwd_workspace_size(B, H, T, d))
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, T, d, causal,
+           scale, stream) -> int:
+    return lib().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, int(workspace_bytes), B,
+                        H, T, d, int(bool(causal)), float(scale), stream)
+
+
+def fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, T, d,
+              causal, scale, status, timeout_ns, flags, stream) -> int:
+    return lib().fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, int(workspace_bytes),
+                           B, H, T, d, int(bool(causal)), float(scale), status,
+                           int(timeout_ns), int(flags), stream)

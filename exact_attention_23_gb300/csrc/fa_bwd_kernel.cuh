@@ -1,0 +1,516 @@
+// Exact attention backward for GB300 (sm_103a): the gradients dQ, dK, dV of
+// O = softmax(scale·QKᵀ [+causal mask])·V for an upstream gradient dO.
+//
+// The forward keeps only the row logsumexp LSE; the backward recomputes the scores and
+// probabilities block by block from it instead of storing the T×T matrix, as step ④ of
+// "手写 FlashAttention" (Hand-written FlashAttention, learn-llm.fim.ai ch. 19) and §2.2 of
+// "FlashAttention 核心思路解析" (FlashAttention core ideas, ijyty.com: recompute per block,
+// sum the per-block query gradients into the global gradient with atomic adds) describe.
+// With D_i = Σ_c dO_ic·O_ic, for a query tile i and key tile j:
+//
+//   Pᵀ  = exp2(log2(e)·scale·K_j·Q_iᵀ − log2(e)·LSE_i)   (keys on TMEM lanes)
+//   dPᵀ = V_j·dO_iᵀ
+//   dSᵀ = Pᵀ ∘ (dPᵀ − D_i)
+//   dV_j += Pᵀ·dO_i      dK_j += dSᵀ·Q_i      dQ_i += dS·K_j   (dK, dQ × scale at the end)
+//
+// Three kernels per call:
+//   fa_bwd_prep_kernel   D_i, log2(e)·LSE_i (+∞ on padding rows, so their P is 0) and a
+//                        zeroed fp32 dQ accumulator, all in the caller's workspace;
+//   fa_bwd_main_kernel   one CTA per (128-key tile j, batch·head), walking the query tiles
+//                        the mask leaves visible; dK_j, dV_j stay in TMEM for the whole walk,
+//                        dQ_i partials are added to the accumulator;
+//   fa_bwd_dq_kernel     accumulator × scale → bf16 dQ.
+//
+// Main kernel, 448 threads, 14 warps:
+//   warps 0-3   compute warpgroup for query columns 0-63 of each tile (thread = key row)
+//   warps 4-7   compute warpgroup for query columns 64-127
+//   warps 8-11  dQ drain: TMEM → registers → vector fp32 atomic adds (thread = query row)
+//   warp  12    MMA issuer (one elected thread); TMEM owner
+//   warp  13    TMA producer
+// Pᵀ and dSᵀ are written once to shared memory as bf16 in the 128-byte-swizzled layout a
+// TMA load would produce ([key row][64 query columns] boxes). The same bytes serve as a
+// K-major A operand (rows = keys: dV, dK) and as an MN-major A operand (dS with queries on
+// M: dQ), so no transpose is ever materialised.
+// Tensor memory (D = 64): [0,128) Sᵀ, [128,256) dPᵀ, [256,320) dV, [320,384) dK,
+// [384,448) and [448,512) two dQ buffers, so one tile's dQ drains while the next is made.
+#pragma once
+
+#include "sm103.cuh"
+
+namespace fa {
+
+constexpr int kBwdThreads = 448;
+constexpr int kBwdDrainWarp0 = 8;
+constexpr int kBwdMmaWarp = 12;
+constexpr int kBwdLoadWarp = 13;
+
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64, "the backward kernel is built for head dim 64");
+  static constexpr int kBox = 128 * 64 * 2;           // one 128-row × 64-col bf16 box = 16 KB
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kStages = 2;                   // (Q_i, dO_i) ring depth
+  static constexpr int kStage0 = kV + kTileBytes;     // stage s: Q at +0, dO at +kTileBytes
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kP = kStage0 + kStages * kStageBytes;  // Pᵀ: 2 boxes (query halves)
+  static constexpr int kDS = kP + 2 * kBox;                    // dSᵀ: 2 boxes
+  static constexpr int kVec = kDS + 2 * kBox;         // stage s: lse2[128] then D[128] (fp32)
+  static constexpr int kBar = kVec + kStages * 1024;
+  static constexpr int kSmemBytes = kBar + 256 + 1024;  // barriers + 1 KB alignment slack
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  static __device__ __forceinline__ constexpr uint32_t col_dq(int b) {
+    return 256u + 2u * D + static_cast<uint32_t>(b) * D;
+  }
+};
+
+struct BwdBars {
+  uint64_t kv_full;     // K_j, V_j landed
+  uint64_t q_full[2];   // Q_i, dO_i, lse2_i, D_i landed in a stage
+  uint64_t q_empty[2];  // every MMA reading that stage is done (tensor core -> producer)
+  uint64_t s_full;      // Sᵀ in TMEM
+  uint64_t dp_full;     // dPᵀ in TMEM
+  uint64_t p_full;      // Pᵀ in shared memory (8 compute warps); also: Sᵀ read out
+  uint64_t p_free;      // dV MMA done with Pᵀ
+  uint64_t ds_full;     // dSᵀ in shared memory (8 compute warps); also: dPᵀ read out
+  uint64_t ds_free;     // dK and dQ MMAs done with dSᵀ
+  uint64_t dq_full[2];  // a dQ partial in TMEM buffer b
+  uint64_t dq_free[2];  // drained (4 drain warps)
+  uint64_t acc_done;    // every MMA of the CTA done: dK, dV final
+  uint32_t tmem_base;
+  uint32_t abort;
+  uint32_t never;       // stays 0: abort flag of the teardown waits, which must not be cut short
+};
+static_assert(sizeof(BwdBars) <= 256, "barrier block");
+
+struct BwdParams {
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const float* lse2;   // [BH][T_pad] log2(e)·LSE, +∞ on padding rows
+  const float* dvec;   // [BH][T_pad] D_i, 0 on padding rows
+  float* dq_acc;       // [BH][n_qt][D/4][128][4] fp32 dQ accumulator (unscaled)
+  int* status;
+  int T;
+  int T_pad;           // n_qt · 128
+  int BH;
+  int n_qt;            // ceil(T / 128): query tiles = key tiles
+  float scale;
+  float scale_log2;    // scale · log2(e)
+  uint64_t timeout_ns;
+  uint32_t flags;
+};
+
+constexpr uint32_t kBwdFlagStarveQ = 1u;  // FA_FLAG_TEST_STARVE_Q
+
+// Offset (in floats) of query row r, columns 4·c4 .. 4·c4+3 of tile (bh, i) in the dQ
+// accumulator. The layout puts the 128 rows of one 4-column group next to each other so
+// that a warp's 32 vector adds cover 512 contiguous bytes.
+__host__ __device__ __forceinline__ size_t dq_acc_offset(int bh, int i, int n_qt, int c4, int r,
+                                                         int d) {
+  return ((((size_t)bh * n_qt + i) * (size_t)(d / 4) + c4) * 128u + r) * 4u;
+}
+
+// ------------------------------------------------------------------------------------
+// Preprocessing: D_i = Σ_c dO_ic·O_ic, lse2_i = log2(e)·LSE_i; zero the dQ accumulator.
+// D/8 consecutive lanes share a row, each reading 8 columns (16 bytes) of O and dO.
+// ------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                                          const __nv_bfloat16* __restrict__ dout,
+                                                          const float* __restrict__ lse,
+                                                          float* __restrict__ lse2,
+                                                          float* __restrict__ dvec,
+                                                          float* __restrict__ dq_acc, int T,
+                                                          int T_pad, int BH) {
+  constexpr int L = D / 8;
+  const size_t nrows = (size_t)BH * T_pad;
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  // T_pad is a multiple of 128, so nrows·L is a multiple of 32 and every lane of a warp
+  // runs the same number of iterations (the shuffles below need the whole warp).
+  for (size_t idx = tid; idx < nrows * L; idx += stride) {
+    const size_t row = idx / L;
+    const int c = static_cast<int>(idx % L);
+    const int bh = static_cast<int>(row / T_pad);
+    const int t = static_cast<int>(row % T_pad);
+    float acc = 0.f;
+    if (t < T) {
+      const size_t off = ((size_t)bh * T + t) * D + (size_t)c * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(o + off);
+      const uint4 b = *reinterpret_cast<const uint4*>(dout + off);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[e]));
+        const float2 fb2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bv[e]));
+        acc = fmaf(fa2.x, fb2.x, acc);
+        acc = fmaf(fa2.y, fb2.y, acc);
+      }
+    }
+#pragma unroll
+    for (int w = L / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+    if (c == 0) {
+      dvec[row] = (t < T) ? acc : 0.f;
+      lse2[row] = (t < T) ? lse[(size_t)bh * T + t] * 1.4426950408889634f : __int_as_float(0x7f800000);
+    }
+  }
+  float4* acc4 = reinterpret_cast<float4*>(dq_acc);
+  const size_t n4 = nrows * (D / 4);
+  for (size_t x = tid; x < n4; x += stride) acc4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ------------------------------------------------------------------------------------
+// dQ = scale · accumulator, as bf16 rows. One thread per (tile, 8 columns, row).
+// ------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ dq_acc,
+                                                        __nv_bfloat16* __restrict__ dq, int T,
+                                                        int n_qt, int BH, float scale) {
+  constexpr int C8 = D / 8;
+  const size_t total = (size_t)BH * n_qt * C8 * 128;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    const int r = static_cast<int>(idx % 128);
+    const size_t rest = idx / 128;
+    const int c8 = static_cast<int>(rest % C8);
+    const size_t tile = rest / C8;  // bh · n_qt + i
+    const int i = static_cast<int>(tile % n_qt);
+    const int bh = static_cast<int>(tile / n_qt);
+    const int t = i * 128 + r;
+    if (t >= T) continue;
+    const float4 a = *reinterpret_cast<const float4*>(dq_acc + dq_acc_offset(bh, i, n_qt, 2 * c8, r, D));
+    const float4 b = *reinterpret_cast<const float4*>(dq_acc + dq_acc_offset(bh, i, n_qt, 2 * c8 + 1, r, D));
+    uint4 out;
+    out.x = pack_bf16x2(a.x * scale, a.y * scale);
+    out.y = pack_bf16x2(a.z * scale, a.w * scale);
+    out.z = pack_bf16x2(b.x * scale, b.y * scale);
+    out.w = pack_bf16x2(b.z * scale, b.w * scale);
+    *reinterpret_cast<uint4*>(dq + ((size_t)bh * T + t) * D + (size_t)c8 * 8) = out;
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Main kernel.
+// ------------------------------------------------------------------------------------
+// Stores 8 fp32 values of one row as bf16 into a 128-byte-swizzled box: 16-byte chunk
+// `ch` of row `r` sits at chunk position ch ^ (r mod 8), as a TMA load would place it.
+__device__ __forceinline__ void st_row_chunk_sw128(uint32_t box, int r, int ch, const float* x) {
+  st_shared_v4(box + static_cast<uint32_t>(r) * 128u + (static_cast<uint32_t>(ch ^ (r & 7)) << 4),
+               pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+               pack_bf16x2(x[6], x[7]));
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  BwdBars* bars = reinterpret_cast<BwdBars*>(sm + C::kBar);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // Heaviest units first: under the causal mask key tile j sees n_qt − j query tiles.
+  const int j = blockIdx.x / p.BH;
+  const int bh = blockIdx.x % p.BH;
+  const int i0 = CAUSAL ? j : 0;
+  const int n = p.n_qt - i0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
+      mbar_init(&bars->dq_full[s], 1);
+      mbar_init(&bars->dq_free[s], 4);
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->p_full, 8);
+    mbar_init(&bars->p_free, 1);
+    mbar_init(&bars->ds_full, 8);
+    mbar_init(&bars->ds_free, 1);
+    mbar_init(&bars->acc_done, 1);
+    bars->abort = 0u;
+    bars->never = 0u;
+    fence_mbar_init();
+  }
+  if (warp == kBwdMmaWarp) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+  const WaitCtl wc{&bars->abort, p.status, p.timeout_ns};
+  const WaitCtl drain_wc{&bars->never, nullptr, p.timeout_ns};
+  const uint32_t sbase = smem_u32(sm);
+
+  if (warp == kBwdLoadWarp) {
+    // ---------------------------------------------------------------- TMA producer
+    int last_t[2] = {-1, -1};
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTileBytes);
+#pragma unroll
+      for (int b = 0; b < D / 64; ++b) {
+        tma_load_3d(sm + C::kK + b * C::kBox, &tm_k, &bars->kv_full, b * 64, j * 128, bh);
+        tma_load_3d(sm + C::kV + b * C::kBox, &tm_v, &bars->kv_full, b * 64, j * 128, bh);
+      }
+    }
+    __syncwarp();
+    const bool starve = (p.flags & kBwdFlagStarveQ) != 0u;
+    for (int t = 0; t < n && !starve; ++t) {
+      const int st = t & 1;
+      if (t >= 2 && !mbar_wait_warp(&bars->q_empty[st], ((t >> 1) - 1) & 1, wc)) break;
+      if (lane == 0) {
+        const int i = i0 + t;
+        uint8_t* stage = sm + C::kStage0 + st * C::kStageBytes;
+        float* vec = reinterpret_cast<float*>(sm + C::kVec + st * 1024);
+        mbar_arrive_expect_tx(&bars->q_full[st], 2 * C::kTileBytes + 1024);
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b) {
+          tma_load_3d(stage + b * C::kBox, &tm_q, &bars->q_full[st], b * 64, i * 128, bh);
+          tma_load_3d(stage + C::kTileBytes + b * C::kBox, &tm_do, &bars->q_full[st], b * 64,
+                      i * 128, bh);
+        }
+        const size_t row0 = (size_t)bh * p.T_pad + (size_t)i * 128;
+        bulk_load(vec, p.lse2 + row0, 512, &bars->q_full[st]);
+        bulk_load(vec + 128, p.dvec + row0, 512, &bars->q_full[st]);
+      }
+      last_t[st] = t;
+      __syncwarp();
+    }
+    // No copy may still be in flight when the CTA exits.
+    mbar_wait_warp(&bars->kv_full, 0, drain_wc);
+    for (int s = 0; s < 2; ++s)
+      if (last_t[s] >= 0) mbar_wait_warp(&bars->q_full[s], (last_t[s] >> 1) & 1, drain_wc);
+  } else if (warp == kBwdMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    constexpr uint32_t kIdS = idesc_bf16(128, 128, false);          // Sᵀ, dPᵀ
+    constexpr uint32_t kIdKV = idesc_bf16_ab(128, D, false, true);  // dV, dK: B MN-major
+    constexpr uint32_t kIdQ = idesc_bf16_ab(128, D, true, true);    // dQ: A and B MN-major
+    const uint32_t k_s = sbase + C::kK, v_s = sbase + C::kV;
+    const uint32_t p_s = sbase + C::kP, ds_s = sbase + C::kDS;
+    auto q_s = [&](int st) { return sbase + C::kStage0 + st * C::kStageBytes; };
+    auto do_s = [&](int st) { return q_s(st) + C::kTileBytes; };
+    // Operand steps: K-major, 16 columns = 32 bytes inside a 64-column box, next box 16 KB
+    // on; MN-major, 16 rows = 2 KB, boxes along M/N 16 KB apart (leading byte offset).
+    auto kmaj = [&](uint32_t base, int kk) {
+      return sdesc_sw128(base + (kk >> 2) * C::kBox + (kk & 3) * 32, 16, 1024);
+    };
+    auto mnmaj = [&](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, C::kBox, 1024); };
+    auto issue_s = [&](int st) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss(tmem + C::kColS, kmaj(k_s, kk), kmaj(q_s(st), kk), kIdS, kk > 0);
+      mma_commit(&bars->s_full);
+    };
+    auto issue_dp = [&](int st) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss(tmem + C::kColDP, kmaj(v_s, kk), kmaj(do_s(st), kk), kIdS, kk > 0);
+      mma_commit(&bars->dp_full);
+    };
+    bool ok = mbar_wait_warp(&bars->kv_full, 0, wc) && mbar_wait_warp(&bars->q_full[0], 0, wc);
+    if (ok) {
+      tc_fence_after_sync();
+      if (lane == 0) {
+        issue_s(0);
+        issue_dp(0);
+      }
+      __syncwarp();
+    }
+    for (int t = 0; t < n && ok; ++t) {
+      const int st = t & 1;
+      // dV += Pᵀ·dO_i
+      if (!(ok = mbar_wait_warp(&bars->p_full, t & 1, wc))) break;
+      tc_fence_after_sync();
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + C::kColDV, kmaj(p_s, kk), mnmaj(do_s(st), kk), kIdKV, (t > 0 || kk > 0));
+        mma_commit(&bars->p_free);
+      }
+      __syncwarp();
+      // the next Sᵀ (Sᵀ_t has been read: Pᵀ_t exists)
+      if (t + 1 < n) {
+        if (!(ok = mbar_wait_warp(&bars->q_full[(t + 1) & 1], ((t + 1) >> 1) & 1, wc))) break;
+        if (lane == 0) issue_s((t + 1) & 1);
+        __syncwarp();
+      }
+      // dK += dSᵀ·Q_i, then dQ_i = dS·K_j
+      if (!(ok = mbar_wait_warp(&bars->ds_full, t & 1, wc))) break;
+      const int b = t & 1;
+      if (t >= 2 && !(ok = mbar_wait_warp(&bars->dq_free[b], ((t >> 1) - 1) & 1, wc))) break;
+      tc_fence_after_sync();
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + C::kColDK, kmaj(ds_s, kk), mnmaj(q_s(st), kk), kIdKV, (t > 0 || kk > 0));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + C::col_dq(b), mnmaj(ds_s, kk), mnmaj(k_s, kk), kIdQ, kk > 0);
+        mma_commit(&bars->dq_full[b]);
+        mma_commit(&bars->ds_free);
+        mma_commit(&bars->q_empty[st]);
+        if (t + 1 < n) issue_dp((t + 1) & 1);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) mma_commit(&bars->acc_done);
+    __syncwarp();
+    // Nothing may be in flight on the tensor core when TMEM is released.
+    mbar_wait_warp(&bars->acc_done, 0, drain_wc);
+  } else if (warp >= kBwdDrainWarp0) {
+    // ---------------------------------------------------------------- dQ drain
+    const int qd = warp & 3;
+    const int r = qd * 32 + lane;  // query row within the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    int t = 0;
+    bool ok = true;
+    for (; t < n; ++t) {
+      const int b = t & 1;
+      if (!(ok = mbar_wait_warp(&bars->dq_full[b], (t >> 1) & 1, wc))) break;
+      tc_fence_after_sync();
+      uint32_t x[D];
+#pragma unroll
+      for (int h = 0; h < D / 32; ++h) tmem_ld32(tmem + lane_off + C::col_dq(b) + h * 32, x + h * 32);
+      tmem_ld_wait();
+#pragma unroll
+      for (int h = 0; h < D / 32; ++h) reg_fence32(x + h * 32);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->dq_free[b]);
+      float* dst = p.dq_acc + dq_acc_offset(bh, i0 + t, p.n_qt, 0, r, D);
+#pragma unroll
+      for (int c4 = 0; c4 < D / 4; ++c4)
+        red_add_v4(dst + (size_t)c4 * 512, __uint_as_float(x[4 * c4]), __uint_as_float(x[4 * c4 + 1]),
+                   __uint_as_float(x[4 * c4 + 2]), __uint_as_float(x[4 * c4 + 3]));
+    }
+    if (!ok) {
+      // Abandoned tiles: poison their dQ rows so that the failure cannot go unseen.
+      const float nan = __int_as_float(0x7fc00000);
+      for (; t < n; ++t) {
+        float* dst = p.dq_acc + dq_acc_offset(bh, i0 + t, p.n_qt, 0, r, D);
+        for (int c4 = 0; c4 < D / 4; ++c4) red_add_v4(dst + (size_t)c4 * 512, nan, nan, nan, nan);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- compute (warps 0-7)
+    const int g = warp >> 2;          // query half: columns 64g .. 64g+63 of each tile
+    const int qd = warp & 3;
+    const int r = qd * 32 + lane;     // key row within the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    const uint32_t p_box = sbase + C::kP + g * C::kBox;
+    const uint32_t ds_box = sbase + C::kDS + g * C::kBox;
+    bool ok = true;
+    for (int t = 0; t < n && ok; ++t) {
+      const int st = t & 1;
+      const int i = i0 + t;
+      const float* vec = reinterpret_cast<const float*>(sm + C::kVec + st * 1024);
+      if (!(ok = mbar_wait_warp(&bars->q_full[st], (t >> 1) & 1, wc))) break;
+      if (!(ok = mbar_wait_warp(&bars->s_full, t & 1, wc))) break;
+      tc_fence_after_sync();
+      uint32_t s[64];
+      tmem_ld32(tmem + lane_off + C::kColS + g * 64, s);
+      tmem_ld32(tmem + lane_off + C::kColS + g * 64 + 32, s + 32);
+      tmem_ld_wait();
+      reg_fence32(s);
+      reg_fence32(s + 32);
+      // Pᵀ = exp2(S·scale·log2e − lse2_q), zero above the diagonal (key > query)
+      float pr[64];
+      const float4* l4 = reinterpret_cast<const float4*>(vec + g * 64);
+#pragma unroll
+      for (int c = 0; c < 64; c += 4) {
+        const float4 l = l4[c / 4];
+        pr[c] = ex2_approx(fmaf(__uint_as_float(s[c]), p.scale_log2, -l.x));
+        pr[c + 1] = ex2_approx(fmaf(__uint_as_float(s[c + 1]), p.scale_log2, -l.y));
+        pr[c + 2] = ex2_approx(fmaf(__uint_as_float(s[c + 2]), p.scale_log2, -l.z));
+        pr[c + 3] = ex2_approx(fmaf(__uint_as_float(s[c + 3]), p.scale_log2, -l.w));
+      }
+      if (CAUSAL && i == j) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (r > g * 64 + c) pr[c] = 0.f;
+      }
+      if (t >= 1 && !(ok = mbar_wait_warp(&bars->p_free, (t - 1) & 1, wc))) break;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) st_row_chunk_sw128(p_box, r, ch, pr + ch * 8);
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full);
+      // dSᵀ = Pᵀ ∘ (dPᵀ − D_q)
+      if (!(ok = mbar_wait_warp(&bars->dp_full, t & 1, wc))) break;
+      if (t >= 1 && !(ok = mbar_wait_warp(&bars->ds_free, (t - 1) & 1, wc))) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t dp[32];
+        tmem_ld32(tmem + lane_off + C::kColDP + g * 64 + h * 32, dp);
+        tmem_ld_wait();
+        reg_fence32(dp);
+        const float4* d4 = reinterpret_cast<const float4*>(vec + 128 + g * 64 + h * 32);
+        float ds[32];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float4 dd = d4[c / 4];
+          ds[c] = pr[h * 32 + c] * (__uint_as_float(dp[c]) - dd.x);
+          ds[c + 1] = pr[h * 32 + c + 1] * (__uint_as_float(dp[c + 1]) - dd.y);
+          ds[c + 2] = pr[h * 32 + c + 2] * (__uint_as_float(dp[c + 2]) - dd.z);
+          ds[c + 3] = pr[h * 32 + c + 3] * (__uint_as_float(dp[c + 3]) - dd.w);
+        }
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) st_row_chunk_sw128(ds_box, r, h * 4 + ch, ds + ch * 8);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->ds_full);
+    }
+    // ---- epilogue: warpgroup 0 writes dV_j, warpgroup 1 writes scale·dK_j
+    const bool done = ok && mbar_wait_warp(&bars->acc_done, 0, wc) && !bars->abort;
+    const int key = j * 128 + r;
+    tc_fence_after_sync();
+    uint32_t x[D];
+    const uint32_t col = (g == 0) ? C::kColDV : C::kColDK;
+#pragma unroll
+    for (int h = 0; h < D / 32; ++h)
+      if (done) tmem_ld32(tmem + lane_off + col + h * 32, x + h * 32);
+    if (done) tmem_ld_wait();
+#pragma unroll
+    for (int h = 0; h < D / 32; ++h) reg_fence32(x + h * 32);
+    const float mul = (g == 0) ? 1.f : p.scale;
+    const float nan = __int_as_float(0x7fc00000);
+    if (key < p.T) {
+      __nv_bfloat16* dst = ((g == 0) ? p.dv : p.dk) + ((size_t)bh * p.T + key) * D;
+#pragma unroll
+      for (int c = 0; c < D; c += 8) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = done ? __uint_as_float(x[c + e]) * mul : nan;
+        uint4 v;
+        v.x = pack_bf16x2(y[0], y[1]);
+        v.y = pack_bf16x2(y[2], y[3]);
+        v.z = pack_bf16x2(y[4], y[5]);
+        v.w = pack_bf16x2(y[6], y[7]);
+        *reinterpret_cast<uint4*>(dst + c) = v;
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kBwdMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace fa

@@ -1,10 +1,11 @@
 // Internal interface between the host API (fa_api.cu) and the kernel instantiations
-// (fa_fwd_d64.cu, fa_fwd_d128.cu). Not part of the public ABI.
+// (fa_fwd_d64.cu, fa_fwd_d128.cu, fa_bwd_d64.cu). Not part of the public ABI.
 #pragma once
 
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa_bwd_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -21,5 +22,21 @@ struct FwdLaunch {
 // Each returns the CUDA error of the launch (cudaSuccess when enqueued).
 cudaError_t launch_fwd_d64(const FwdLaunch& a, bool causal);
 cudaError_t launch_fwd_d128(const FwdLaunch& a, bool causal);
+
+struct BwdLaunch {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  BwdParams p;
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dout;
+  const float* lse;
+  float* lse2;
+  float* dvec;
+  __nv_bfloat16* dq;
+  unsigned grid_main, grid_prep, grid_dq;
+  cudaStream_t stream;
+};
+
+// Enqueues the three backward kernels (prep, main, dQ conversion) on a.stream.
+cudaError_t launch_bwd_d64(const BwdLaunch& a, bool causal);
 
 }  // namespace fa

@@ -165,6 +165,37 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// Plain (untiled) bulk copy global -> shared of `bytes` bytes (both addresses 16-byte
+// aligned, bytes a multiple of 16), completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Makes this thread's earlier generic-proxy shared-memory writes visible to the async
+// proxy (tensor-core operand reads), to be followed by a barrier arrive.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// Four fp32 atomically added to 16-byte-aligned global memory (no return value).
+__device__ __forceinline__ void red_add_v4(float* gaddr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gaddr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
 // ------------------------------------------------------------------------------------
 // tcgen05: TMEM allocation, MMA, commit, loads/stores, fences
 // ------------------------------------------------------------------------------------
@@ -229,6 +260,12 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Same with both operand majors explicit (A MN-major sets bit 15).
+__host__ __device__ constexpr uint32_t idesc_bf16_ab(uint32_t M, uint32_t N, bool a_mn_major,
+                                                     bool b_mn_major) {
+  return idesc_bf16(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.

@@ -8,7 +8,9 @@ v with ``randn`` in fp32 (shape [B, H, T, d]); each is multiplied by ``std`` and
 bf16 with round-to-nearest-even. For the "spiky" workload one key row per (b, h),
 at an index drawn afterwards from the same generator uniformly in [128, T), is
 multiplied by 8 in fp32 before the cast, so that every query that sees that key meets
-a large jump of the running row max in the middle of its scan. The pages' workloads
+a large jump of the running row max in the middle of its scan. The upstream gradient dO
+of a backward test comes from a second generator seeded with seed + 1_000_003, drawn
+with ``randn`` in fp32 and cast to bf16 the same way. The pages' workloads
 use random bf16 q/k/v at GPT-2 124M head shapes (12 heads of width 64) and a length
 sweep up to 16k ("Hand-written FlashAttention", steps ④ and ⑤).
 """
@@ -87,3 +89,15 @@ def workload_qkv(w: Workload):
 def to_f64_numpy(t: torch.Tensor):
     """Exact bf16 → fp64 numpy view for the oracle (bf16 values are exact in fp64)."""
     return t.detach().to("cpu", torch.float64).numpy()
+
+
+def make_do(B: int, H: int, T: int, d: int, seed: int):
+    """Draw the upstream gradient dO ([B, H, T, d] bf16, standard normal) for a backward
+    test of the workload with this seed."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 1_000_003)
+    return torch.randn((B, H, T, d), generator=g, dtype=torch.float32).to(torch.bfloat16).contiguous()
+
+
+def workload_do(w: Workload):
+    return make_do(w.B, w.H, w.T, w.d, w.seed)

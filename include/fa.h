@@ -1,5 +1,6 @@
 /*
- * fa.h — C ABI of the GB300 (sm_103a) exact attention forward library, libfa.so.
+ * fa.h — C ABI of the GB300 (sm_103a) exact attention library, libfa.so: the forward
+ * pass (fa_fwd) and its gradient (fa_bwd, further down).
  *
  * The operation, for every batch b and head h of contiguous [B, H, T, d] tensors:
  *
@@ -35,6 +36,8 @@
  */
 #ifndef FA_GB300_FA_H_
 #define FA_GB300_FA_H_
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -84,6 +87,68 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
               int T, int d, int causal, float scale, int* status, unsigned long long timeout_ns,
               unsigned int flags, void* stream);
+
+/*
+ * ---------------------------------------------------------------------------------------
+ * Backward pass.
+ *
+ * The gradients of the forward above for an upstream gradient dO = ∂L/∂O:
+ *
+ *     P     = exp(S − LSE)            (recomputed from q, k and the forward's lse)
+ *     dV    = Pᵀ dO
+ *     dP    = dO Vᵀ,   D_i = Σ_c dO_ic O_ic
+ *     dS    = P ∘ (dP − D)
+ *     dQ    = scale · dS K,   dK = scale · dSᵀ Q
+ *
+ * Step ④ of "手写 FlashAttention" (Hand-written FlashAttention) explains why the forward
+ * keeps the row logsumexp: so that the backward can rebuild S and P block by block
+ * instead of storing them; §2.2 of "FlashAttention 核心思路解析" (FlashAttention core
+ * ideas, ijyty.com) adds that the per-block query gradients are summed into the global
+ * gradient with atomic adds. Neither page writes out the derivative; the formulas above
+ * are the chain rule applied to the forward's definition.
+ * ---------------------------------------------------------------------------------------
+ */
+
+/*
+ * fa_bwd_workspace_size — bytes of device workspace that fa_bwd needs for these sizes
+ * (fp32 row statistics and an fp32 dQ accumulator: about B·H·T·(d + 2)·4 bytes).
+ * Returns 0 when the sizes are not supported by fa_bwd (currently d must be 64).
+ */
+size_t fa_bwd_workspace_size(int B, int H, int T, int d);
+
+/*
+ * fa_bwd — exact attention backward.
+ *
+ *   q, k, v   : const bf16*, [B, H, T, d], device memory: the forward's inputs
+ *   o         : const bf16*, [B, H, T, d]: the forward's output
+ *   dout      : const bf16*, [B, H, T, d]: the upstream gradient dO
+ *   lse       : const float*, [B, H, T]: the forward's lse
+ *   dq, dk, dv: bf16*, [B, H, T, d], device memory, written
+ *   workspace : device memory owned by the caller, at least fa_bwd_workspace_size(...)
+ *               bytes, 256-byte aligned; its contents on entry do not matter (the call
+ *               initialises what it uses). It must not be used by another call that may
+ *               run at the same time.
+ *   causal, scale, stream : as for fa_fwd, and equal to the values of the forward call.
+ *
+ * Supported: d = 64; otherwise as fa_fwd. dq, dk, dv and the workspace must not overlap
+ * any input or one another. The call enqueues three kernels on `stream` and returns; the
+ * library allocates nothing. Returns FA_OK or an fa_status code (host-side validation
+ * as for fa_fwd; nothing is launched on failure).
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, void* workspace,
+           size_t workspace_bytes, int B, int H, int T, int d, int causal, float scale,
+           void* stream);
+
+/*
+ * fa_bwd_ex — fa_bwd with the fault-reporting controls of fa_fwd_ex: a timed-out internal
+ * wait stores FA_ERR_TIMEOUT in *status and leaves NaN in the dq, dk, dv rows of the
+ * abandoned work; flag FA_FLAG_TEST_STARVE_Q omits the query-tile and dO loads (test only).
+ */
+int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
+              const float* lse, void* dq, void* dk, void* dv, void* workspace,
+              size_t workspace_bytes, int B, int H, int T, int d, int causal, float scale,
+              int* status, unsigned long long timeout_ns, unsigned int flags, void* stream);
 
 /* Static text for a status code (never NULL). */
 const char* fa_strerror(int status);

@@ -20,6 +20,7 @@ from .naive import (  # noqa: F401
     attention_backward,
     attention_backward_cols,
     attention_backward_head,
+    attention_backward_magnitudes,
     attention_backward_rows,
     attention_rows,
     online_softmax_trace,

@@ -305,3 +305,47 @@ def attention_backward(q, k, v, do, causal: bool, scale: float):
             dq[b, h], dk[b, h], dv[b, h] = attention_backward_head(
                 q[b, h], k[b, h], v[b, h], do[b, h], causal, scale)
     return dq, dk, dv
+
+
+def attention_backward_magnitudes(q, k, v, do, causal: bool, scale: float,
+                                  row_chunk: int = 512):
+    """Error-bound magnitudes of the backward's sums, per output element.
+
+    A sum Σ a_j·b_j whose terms each carry a relative error ≤ u is off by at most
+    u·Σ|a_j|·|b_j| (the usual floating-point bound). An implementation that rounds P and
+    dS to a short format and forms D = Σ_c dO_c·O_c from a rounded O perturbs dS_ij by up
+    to u·A_ij with
+
+        A_ij = |dS_ij| + P_ij·Σ_c |dO_ic|·(|O_ic| + |V_jc|)
+
+    (the second term: the rounding of O inside D, and of dP = dO·V_j). So the sums are
+    bounded through
+
+        M_dV = Pᵀ·|dO|,   M_dK = scale·Aᵀ·|Q|,   M_dQ = scale·A·|K|.
+
+    Arrays as attention_backward."""
+    q = _as_f64(q)
+    k = _as_f64(k)
+    v = _as_f64(v)
+    do = _as_f64(do)
+    B, H, T, d = q.shape
+    mq = np.empty_like(q)
+    mk = np.zeros_like(k)
+    mv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            for r0 in range(0, T, row_chunk):
+                rows = np.arange(r0, min(T, r0 + row_chunk))
+                s = scores(q[b, h, rows], k[b, h], scale)
+                if causal:
+                    s = apply_causal_mask(s, rows)
+                p, _, _ = safe_softmax(s)
+                o_rows = weighted_values(p, v[b, h])
+                ado = np.abs(do[b, h, rows])
+                a = np.abs(softmax_backward(p, grad_probs(do[b, h, rows], v[b, h])))
+                a += p * (np.sum(ado * np.abs(o_rows), axis=1, keepdims=True)
+                          + ado @ np.abs(v[b, h]).T)
+                mv[b, h] += p.T @ ado
+                mq[b, h, rows] = scale * (a @ np.abs(k[b, h]))
+                mk[b, h] += scale * (a.T @ np.abs(q[b, h, rows]))
+    return mq, mk, mv

@@ -377,12 +377,28 @@ def pin_bwd_sampled(orc):
         assert np.max(np.abs(dvc - dv[0, 0, rows])) <= 1e-12
 
 
+def pin_bwd_magnitudes(orc):
+    """The error-bound magnitudes dominate the gradients (|Σ a·b| ≤ Σ|a|·|b|), and with
+    dO ≥ 0 the dV magnitude is dV itself (P ≥ 0, so no term changes sign)."""
+    q, k, v = _qkv(27, 1, 2, 70, 6)
+    do = _rng(28).standard_normal(q.shape)
+    for causal in (False, True):
+        g = orc.attention_backward(q, k, v, do, causal, 0.4)
+        m = orc.attention_backward_magnitudes(q, k, v, do, causal, 0.4)
+        for gi, mi in zip(g, m):
+            assert np.all(mi >= np.abs(gi) - 1e-12)
+        dop = np.abs(do)
+        _, _, dv = orc.attention_backward(q, k, v, dop, causal, 0.4)
+        _, _, mv = orc.attention_backward_magnitudes(q, k, v, dop, causal, 0.4)
+        assert np.max(np.abs(mv - dv)) <= 1e-12
+
+
 ORACLE_PINS = [pin_bruteforce, pin_hand_example, pin_row_sums, pin_constant_v,
                pin_causal_row0, pin_uniform, pin_shift, pin_permutation, pin_large_scores,
                pin_rows_match_full, pin_sdpa_library]
 RECURRENCE_PINS = [pin_online_trace, pin_online_weighted_sum]
 BACKWARD_PINS = [pin_bwd_finite_diff, pin_bwd_hand_example, pin_bwd_invariants,
-                 pin_bwd_autograd, pin_bwd_sampled]
+                 pin_bwd_autograd, pin_bwd_sampled, pin_bwd_magnitudes]
 
 
 def load_page_facts():

@@ -125,3 +125,57 @@ def test_tiling_arithmetic_matches_the_page():
     assert fa.q_tiles(4096, 64) * 4 * 12 == facts["programs_b4_h12_t4096_block64"]
     assert fa.q_tiles(1000) == 8 and fa.q_tiles(128) == 1 and fa.q_tiles(129) == 2
     assert math.ceil(fa.q_tiles(4096) / 2) * 48 == 768
+
+
+# ------------------------------------------------------------------------------ backward
+
+def test_bwd_workspace_size(lib):
+    # [BH][T_pad] lse2 and D (fp32) plus a [BH][T_pad][d] fp32 dQ accumulator, 256-aligned
+    assert fa.fa_bwd_workspace_size(1, 1, 128, 64) == 2 * 512 + 128 * 64 * 4
+    assert fa.fa_bwd_workspace_size(2, 3, 129, 64) == 2 * 6 * 256 * 4 + 6 * 256 * 64 * 4
+    assert fa.fa_bwd_workspace_size(4, 12, 16384, 64) == 48 * 16384 * (2 + 64) * 4
+    assert fa.fa_bwd_workspace_size(1, 1, 1, 64) == 2 * 512 + 128 * 64 * 4
+    for bad in ((0, 1, 128, 64), (1, 0, 128, 64), (1, 1, 0, 64), (1, 1, 128, 128),
+                (1, 1, 128, 32), (1 << 16, 1 << 15, 1 << 16, 64)):
+        assert fa.fa_bwd_workspace_size(*bad) == 0, bad
+
+
+def _bwd_call(q=A, k=A + SZ, v=A + 2 * SZ, o=A + 3 * SZ, do=A + 4 * SZ, lse=A + 5 * SZ,
+              dq=A + 6 * SZ, dk=A + 7 * SZ, dv=A + 8 * SZ, ws=A + 9 * SZ, ws_bytes=None, B=1, H=1,
+              T=128, d=64, causal=1, scale=0.125, flags=0):
+    if ws_bytes is None:
+        ws_bytes = max(fa.fa_bwd_workspace_size(B, H, T, 64), 1 << 20)
+    return fa.fa_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, ws, ws_bytes, B, H, T, d, causal, scale,
+                        None, 0, flags, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(o=0), fa.FA_ERR_INVALID_ARG),
+    (dict(do=0), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=0), fa.FA_ERR_INVALID_ARG),
+    (dict(T=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=128), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(flags=4), fa.FA_ERR_INVALID_ARG),
+    (dict(ws_bytes=1024), fa.FA_ERR_INVALID_ARG),                   # workspace too small
+    (dict(ws=A + 9 * SZ + 16), fa.FA_ERR_MISALIGNED),               # workspace not 256-aligned
+    (dict(dk=A + 7 * SZ + 8), fa.FA_ERR_MISALIGNED),
+    (dict(dq=A), fa.FA_ERR_INVALID_ARG),                            # dq aliases q
+    (dict(dv=A + 6 * SZ + 4096), fa.FA_ERR_INVALID_ARG),            # dv overlaps dq
+    (dict(ws=A + 5 * SZ), fa.FA_ERR_INVALID_ARG),                   # workspace overlaps lse
+])
+def test_bwd_host_validation_rejects_before_launch(lib, kw, want):
+    assert _bwd_call(**kw) == want
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="only meaningful on a machine without a CUDA device")
+def test_bwd_valid_call_without_device_reports_unsupported(lib):
+    assert _bwd_call() == fa.FA_ERR_UNSUPPORTED_DEVICE
+
+
+def test_bwd_flop_count():
+    assert fa.bwd_flops(4, 12, 4096, 64, True) == 2.5 * fa.flops(4, 12, 4096, 64, True)
