@@ -21,10 +21,11 @@ FA_ERR_UNSUPPORTED_DEVICE = 3
 FA_ERR_LAUNCH = 4
 FA_ERR_TIMEOUT = 5
 FA_FLAG_TEST_STARVE_Q = 1
+FA_BWD_NOALLOC_SCRATCH_BYTES = 33554432
 
 # Every symbol include/fa.h declares.
-EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_ex", "fa_strerror",
-           "fa_version")
+EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_ex",
+           "fa_bwd_noalloc", "fa_strerror", "fa_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -59,6 +60,8 @@ def lib() -> ctypes.CDLL:
             L.fa_bwd_ex.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, vp, ctypes.c_ulonglong,
                                                 ctypes.c_uint, vp]
             L.fa_bwd_ex.restype = i
+            L.fa_bwd_noalloc.argtypes = [vp] * 9 + [i, i, i, i, i, f, vp]
+            L.fa_bwd_noalloc.restype = i
             L.fa_strerror.argtypes = [i]
             L.fa_strerror.restype = ctypes.c_char_p
             L.fa_version.argtypes = []
@@ -101,3 +104,8 @@ def fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, 
     return lib().fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, int(workspace_bytes),
                            B, H, T, d, int(bool(causal)), float(scale), status,
                            int(timeout_ns), int(flags), stream)
+
+
+def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, T, d, causal, scale, stream) -> int:
+    return lib().fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, T, d,
+                                int(bool(causal)), float(scale), stream)

@@ -150,6 +150,33 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
               size_t workspace_bytes, int B, int H, int T, int d, int causal, float scale,
               int* status, unsigned long long timeout_ns, unsigned int flags, void* stream);
 
+/*
+ * fa_bwd_noalloc — fa_bwd without a caller-provided workspace. The pages describe no
+ * such call; it exists for callers that cannot give the library a device buffer (their
+ * memory is already committed to their own pools, or they call from a path where a
+ * device allocation is not acceptable).
+ *
+ * The workspace is a fixed reservation of FA_BWD_NOALLOC_SCRATCH_BYTES (32 MiB) of device
+ * memory inside the library, made when the library's device code is loaded onto a
+ * device. The call allocates nothing. Its contents need not start at zero: every call
+ * initialises what it uses.
+ *
+ *   - Sizes whose workspace (fa_bwd_workspace_size) exceeds the reservation are rejected
+ *     with FA_ERR_INVALID_ARG before anything is launched; with d = 64 that is
+ *     B·H·ceil(T/128)·128·66·4 bytes > 32 MiB, e.g. B·H = 12 allows T ≤ 10496.
+ *   - The first call on each device looks up the reservation's device address (which
+ *     may load the library's device code); FA_ERR_LAUNCH if that fails. Make that first
+ *     call before any stream capture on the device.
+ *   - There is one reservation per device: calls that may overlap in time on the same
+ *     device (different streams, or several host threads) race on it and give wrong
+ *     results. Order them on one stream, or with events.
+ *   - Everything else (arguments, layout, validation, asynchrony) as fa_bwd.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES 33554432
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int T, int d,
+                   int causal, float scale, void* stream);
+
 /* Static text for a status code (never NULL). */
 const char* fa_strerror(int status);
 
