@@ -21,28 +21,42 @@
 //                        dQ_i partials are added to the accumulator;
 //   fa_bwd_dq_kernel     accumulator × scale → bf16 dQ.
 //
-// Main kernel, 448 threads, 14 warps:
+// Main kernel, 480 threads, 15 warps:
 //   warps 0-3   compute warpgroup for query columns 0-63 of each tile (thread = key row)
 //   warps 4-7   compute warpgroup for query columns 64-127
 //   warps 8-11  dQ drain: TMEM → registers → vector fp32 atomic adds (thread = query row)
-//   warp  12    MMA issuer (one elected thread); TMEM owner
-//   warp  13    TMA producer
-// Pᵀ and dSᵀ are written once to shared memory as bf16 in the 128-byte-swizzled layout a
-// TMA load would produce ([key row][64 query columns] boxes). The same bytes serve as a
-// K-major A operand (rows = keys: dV, dK) and as an MN-major A operand (dS with queries on
-// M: dQ), so no transpose is ever materialised.
+//   warp  12    score issuer: Sᵀ and dPᵀ MMAs (one elected thread); TMEM owner
+//   warp  13    gradient issuer: dV, dK and dQ MMAs (one elected thread)
+//   warp  14    TMA producer
+// (15 warps leave 128 registers per thread; the compute warps read dPᵀ in two halves to
+// stay within them.)
+// Two issuers, because MMAs into different accumulators are not ordered with one another
+// and a single issuer blocked on one barrier would hold back independent work: the score
+// issuer starts Sᵀ of the next tile as soon as the compute warps have read the current
+// one into registers, while the gradient issuer is still waiting for this tile's Pᵀ/dSᵀ.
+// Pᵀ goes to tensor memory (bf16 pairs, the A operand of the dV MMA). dSᵀ is written to
+// shared memory as bf16 in the 128-byte-swizzled layout a TMA load would produce
+// ([key row][64 query columns] boxes, double-buffered). The same bytes serve as the
+// K-major A operand of dK (rows = keys) and the MN-major A operand of dQ (queries on M),
+// so no transpose is ever materialised.
 // Tensor memory (D = 64): [0,128) Sᵀ, [128,256) dPᵀ, [256,320) dV, [320,384) dK,
-// [384,448) and [448,512) two dQ buffers, so one tile's dQ drains while the next is made.
+// [384,448) dQ, [448,512) Pᵀ (bf16 pairs).
 #pragma once
 
 #include "sm103.cuh"
 
+// Timeline hooks: compiled out unless a tracing build defines FA_TRACE(tag, step).
+#ifndef FA_TRACE
+#define FA_TRACE(tag, step) ((void)0)
+#endif
+
 namespace fa {
 
-constexpr int kBwdThreads = 448;
+constexpr int kBwdThreads = 480;
 constexpr int kBwdDrainWarp0 = 8;
-constexpr int kBwdMmaWarp = 12;
-constexpr int kBwdLoadWarp = 13;
+constexpr int kBwdScoreWarp = 12;
+constexpr int kBwdGradWarp = 13;
+constexpr int kBwdLoadWarp = 14;
 
 template <int D>
 struct BwdCfg {
@@ -51,33 +65,34 @@ struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
-  static constexpr int kStages = 2;                   // (Q_i, dO_i) ring depth
+  static constexpr int kStages = 3;                   // (Q_i, dO_i) ring depth
   static constexpr int kStage0 = kV + kTileBytes;     // stage s: Q at +0, dO at +kTileBytes
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kP = kStage0 + kStages * kStageBytes;  // Pᵀ: 2 boxes (query halves)
-  static constexpr int kDS = kP + 2 * kBox;                    // dSᵀ: 2 boxes
-  static constexpr int kVec = kDS + 2 * kBox;         // stage s: lse2[128] then D[128] (fp32)
+  static constexpr int kDS = kStage0 + kStages * kStageBytes;  // dSᵀ: 2 buffers × 2 boxes
+  static constexpr int kDSBytes = 2 * kBox;
+  static constexpr int kVec = kDS + 2 * kDSBytes;     // stage s: lse2[128] then D[128] (fp32)
   static constexpr int kBar = kVec + kStages * 1024;
   static constexpr int kSmemBytes = kBar + 256 + 1024;  // barriers + 1 KB alignment slack
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
-  static __device__ __forceinline__ constexpr uint32_t col_dq(int b) {
-    return 256u + 2u * D + static_cast<uint32_t>(b) * D;
-  }
+  static constexpr uint32_t kColDQ = 256 + 2 * D, kColP = 448;
 };
 
 struct BwdBars {
   uint64_t kv_full;     // K_j, V_j landed
-  uint64_t q_full[2];   // Q_i, dO_i, lse2_i, D_i landed in a stage
-  uint64_t q_empty[2];  // every MMA reading that stage is done (tensor core -> producer)
+  uint64_t q_full[3];   // Q_i, dO_i, lse2_i, D_i landed in a stage
+  uint64_t q_empty[3];  // both issuers' MMAs reading that stage are done (2 arrivals)
   uint64_t s_full;      // Sᵀ in TMEM
+  uint64_t s_free;      // Sᵀ read into registers (8 compute warps)
   uint64_t dp_full;     // dPᵀ in TMEM
-  uint64_t p_full;      // Pᵀ in shared memory (8 compute warps); also: Sᵀ read out
+  uint64_t dp_free;     // dPᵀ read into registers (8 compute warps)
+  uint64_t p_full;      // Pᵀ stored in TMEM (8 compute warps)
   uint64_t p_free;      // dV MMA done with Pᵀ
-  uint64_t ds_full;     // dSᵀ in shared memory (8 compute warps); also: dPᵀ read out
-  uint64_t ds_free;     // dK and dQ MMAs done with dSᵀ
-  uint64_t dq_full[2];  // a dQ partial in TMEM buffer b
-  uint64_t dq_free[2];  // drained (4 drain warps)
-  uint64_t acc_done;    // every MMA of the CTA done: dK, dV final
+  uint64_t ds_full[2];  // dSᵀ buffer in shared memory (8 compute warps)
+  uint64_t ds_free[2];  // dK and dQ MMAs done with that buffer
+  uint64_t dq_full;     // a dQ partial in TMEM
+  uint64_t dq_free;     // drained (4 drain warps)
+  uint64_t score_done;  // every MMA of the score issuer done
+  uint64_t grad_done;   // every MMA of the gradient issuer done: dK, dV final
   uint32_t tmem_base;
   uint32_t abort;
   uint32_t never;       // stays 0: abort flag of the teardown waits, which must not be cut short
@@ -207,6 +222,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const BwdParams p) {
   using C = BwdCfg<D>;
+  constexpr int NS = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   BwdBars* bars = reinterpret_cast<BwdBars*>(sm + C::kBar);
@@ -219,24 +235,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&bars->q_full[s], 1);
-      mbar_init(&bars->q_empty[s], 1);
-      mbar_init(&bars->dq_full[s], 1);
-      mbar_init(&bars->dq_free[s], 4);
+      mbar_init(&bars->q_empty[s], 2);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->ds_full[s], 8);
+      mbar_init(&bars->ds_free[s], 1);
     }
     mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 8);
     mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->dp_free, 8);
     mbar_init(&bars->p_full, 8);
     mbar_init(&bars->p_free, 1);
-    mbar_init(&bars->ds_full, 8);
-    mbar_init(&bars->ds_free, 1);
-    mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, 4);
+    mbar_init(&bars->score_done, 1);
+    mbar_init(&bars->grad_done, 1);
     bars->abort = 0u;
     bars->never = 0u;
     fence_mbar_init();
   }
-  if (warp == kBwdMmaWarp) {
+  if (warp == kBwdScoreWarp) {
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
@@ -247,10 +268,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const WaitCtl wc{&bars->abort, p.status, p.timeout_ns};
   const WaitCtl drain_wc{&bars->never, nullptr, p.timeout_ns};
   const uint32_t sbase = smem_u32(sm);
+  auto q_s = [&](int st) { return sbase + C::kStage0 + st * C::kStageBytes; };
+  auto do_s = [&](int st) { return q_s(st) + C::kTileBytes; };
+  // Operand steps: K-major, 16 columns = 32 bytes inside a 64-column box, next box 16 KB
+  // on; MN-major, 16 rows = 2 KB, boxes along M/N 16 KB apart (leading byte offset).
+  auto kmaj = [&](uint32_t base, int kk) {
+    return sdesc_sw128(base + (kk >> 2) * C::kBox + (kk & 3) * 32, 16, 1024);
+  };
+  auto mnmaj = [&](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, C::kBox, 1024); };
+  // End of every role (each calls it last, so that no code is shared between warpgroups
+  // that run with different register budgets). Nothing may be in flight on the tensor
+  // core when TMEM is released.
+  auto teardown = [&]() {
+    if (warp == kBwdScoreWarp) {
+      mbar_wait_warp_inl(&bars->score_done, 0, drain_wc);
+      mbar_wait_warp_inl(&bars->grad_done, 0, drain_wc);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kBwdScoreWarp) {
+      tc_fence_after_sync();
+      tmem_dealloc(tmem, 512);
+    }
+  };
 
+  if (warp >= kBwdScoreWarp) {
   if (warp == kBwdLoadWarp) {
     // ---------------------------------------------------------------- TMA producer
-    int last_t[2] = {-1, -1};
+    int last_t[NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) last_t[s] = -1;
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -265,9 +312,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     __syncwarp();
     const bool starve = (p.flags & kBwdFlagStarveQ) != 0u;
-    for (int t = 0; t < n && !starve; ++t) {
-      const int st = t & 1;
-      if (t >= 2 && !mbar_wait_warp(&bars->q_empty[st], ((t >> 1) - 1) & 1, wc)) break;
+    for (int t = 0, st = 0, ph = 0; t < n && !starve; ++t) {
+      if (t >= NS && !mbar_wait_warp_inl(&bars->q_empty[st], ph ^ 1, wc)) break;
+      FA_TRACE(30, t);
       if (lane == 0) {
         const int i = i0 + t;
         uint8_t* stage = sm + C::kStage0 + st * C::kStageBytes;
@@ -285,88 +332,90 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       last_t[st] = t;
       __syncwarp();
+      if (++st == NS) { st = 0; ph ^= 1; }
     }
     // No copy may still be in flight when the CTA exits.
-    mbar_wait_warp(&bars->kv_full, 0, drain_wc);
-    for (int s = 0; s < 2; ++s)
-      if (last_t[s] >= 0) mbar_wait_warp(&bars->q_full[s], (last_t[s] >> 1) & 1, drain_wc);
-  } else if (warp == kBwdMmaWarp) {
-    // ---------------------------------------------------------------- MMA issuer
-    constexpr uint32_t kIdS = idesc_bf16(128, 128, false);          // Sᵀ, dPᵀ
-    constexpr uint32_t kIdKV = idesc_bf16_ab(128, D, false, true);  // dV, dK: B MN-major
-    constexpr uint32_t kIdQ = idesc_bf16_ab(128, D, true, true);    // dQ: A and B MN-major
+    mbar_wait_warp_inl(&bars->kv_full, 0, drain_wc);
+#pragma unroll
+    for (int s = 0; s < NS; ++s)
+      if (last_t[s] >= 0) mbar_wait_warp_inl(&bars->q_full[s], (last_t[s] / NS) & 1, drain_wc);
+  } else if (warp == kBwdScoreWarp) {
+    // ---------------------------------------------------------------- score issuer
+    constexpr uint32_t kIdS = idesc_bf16(128, 128, false);  // Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ
     const uint32_t k_s = sbase + C::kK, v_s = sbase + C::kV;
-    const uint32_t p_s = sbase + C::kP, ds_s = sbase + C::kDS;
-    auto q_s = [&](int st) { return sbase + C::kStage0 + st * C::kStageBytes; };
-    auto do_s = [&](int st) { return q_s(st) + C::kTileBytes; };
-    // Operand steps: K-major, 16 columns = 32 bytes inside a 64-column box, next box 16 KB
-    // on; MN-major, 16 rows = 2 KB, boxes along M/N 16 KB apart (leading byte offset).
-    auto kmaj = [&](uint32_t base, int kk) {
-      return sdesc_sw128(base + (kk >> 2) * C::kBox + (kk & 3) * 32, 16, 1024);
-    };
-    auto mnmaj = [&](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, C::kBox, 1024); };
-    auto issue_s = [&](int st) {
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss(tmem + C::kColS, kmaj(k_s, kk), kmaj(q_s(st), kk), kIdS, kk > 0);
-      mma_commit(&bars->s_full);
-    };
-    auto issue_dp = [&](int st) {
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss(tmem + C::kColDP, kmaj(v_s, kk), kmaj(do_s(st), kk), kIdS, kk > 0);
-      mma_commit(&bars->dp_full);
-    };
-    bool ok = mbar_wait_warp(&bars->kv_full, 0, wc) && mbar_wait_warp(&bars->q_full[0], 0, wc);
-    if (ok) {
+    bool ok = mbar_wait_warp_inl(&bars->kv_full, 0, wc);
+    for (int t = 0, st = 0, ph = 0; t < n && ok; ++t) {
+      if (!(ok = mbar_wait_warp_inl(&bars->q_full[st], ph, wc))) break;
+      if (t > 0 && !(ok = mbar_wait_warp_inl(&bars->s_free, (t - 1) & 1, wc))) break;
+      FA_TRACE(1, t);
       tc_fence_after_sync();
       if (lane == 0) {
-        issue_s(0);
-        issue_dp(0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::kColS, kmaj(k_s, kk), kmaj(q_s(st), kk), kIdS, kk > 0);
+        mma_commit(&bars->s_full);
       }
       __syncwarp();
+      if (t > 0 && !(ok = mbar_wait_warp_inl(&bars->dp_free, (t - 1) & 1, wc))) break;
+      FA_TRACE(2, t);
+      tc_fence_after_sync();
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::kColDP, kmaj(v_s, kk), kmaj(do_s(st), kk), kIdS, kk > 0);
+        mma_commit(&bars->dp_full);
+        mma_commit(&bars->q_empty[st]);
+      }
+      __syncwarp();
+      if (++st == NS) { st = 0; ph ^= 1; }
     }
-    for (int t = 0; t < n && ok; ++t) {
-      const int st = t & 1;
-      // dV += Pᵀ·dO_i
-      if (!(ok = mbar_wait_warp(&bars->p_full, t & 1, wc))) break;
+    if (lane == 0) mma_commit(&bars->score_done);
+    __syncwarp();
+  } else if (warp == kBwdGradWarp) {
+    // ---------------------------------------------------------------- gradient issuer
+    constexpr uint32_t kIdV = idesc_bf16(128, D, true);             // dV: A in TMEM, B MN-major
+    constexpr uint32_t kIdK = idesc_bf16_ab(128, D, false, true);   // dK: A K-major, B MN-major
+    constexpr uint32_t kIdQ = idesc_bf16_ab(128, D, true, true);    // dQ: A and B MN-major
+    const uint32_t k_s = sbase + C::kK;
+    bool ok = true;
+    for (int t = 0, st = 0; t < n && ok; ++t) {
+      // dV += Pᵀ·dO_i (Pᵀ from TMEM)
+      if (!(ok = mbar_wait_warp_inl(&bars->p_full, t & 1, wc))) break;
+      FA_TRACE(3, t);
       tc_fence_after_sync();
       if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::kColDV, kmaj(p_s, kk), mnmaj(do_s(st), kk), kIdKV, (t > 0 || kk > 0));
+          mma_ts(tmem + C::kColDV, tmem + C::kColP + kk * 8, mnmaj(do_s(st), kk), kIdV,
+                 (t > 0 || kk > 0));
         mma_commit(&bars->p_free);
       }
       __syncwarp();
-      // the next Sᵀ (Sᵀ_t has been read: Pᵀ_t exists)
-      if (t + 1 < n) {
-        if (!(ok = mbar_wait_warp(&bars->q_full[(t + 1) & 1], ((t + 1) >> 1) & 1, wc))) break;
-        if (lane == 0) issue_s((t + 1) & 1);
-        __syncwarp();
-      }
       // dK += dSᵀ·Q_i, then dQ_i = dS·K_j
-      if (!(ok = mbar_wait_warp(&bars->ds_full, t & 1, wc))) break;
       const int b = t & 1;
-      if (t >= 2 && !(ok = mbar_wait_warp(&bars->dq_free[b], ((t >> 1) - 1) & 1, wc))) break;
+      const uint32_t ds_s = sbase + C::kDS + b * C::kDSBytes;
+      if (!(ok = mbar_wait_warp_inl(&bars->ds_full[b], (t >> 1) & 1, wc))) break;
+      if (t > 0 && !(ok = mbar_wait_warp_inl(&bars->dq_free, (t - 1) & 1, wc))) break;
+      FA_TRACE(4, t);
       tc_fence_after_sync();
       if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::kColDK, kmaj(ds_s, kk), mnmaj(q_s(st), kk), kIdKV, (t > 0 || kk > 0));
+          mma_ss(tmem + C::kColDK, kmaj(ds_s, kk), mnmaj(q_s(st), kk), kIdK, (t > 0 || kk > 0));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::col_dq(b), mnmaj(ds_s, kk), mnmaj(k_s, kk), kIdQ, kk > 0);
-        mma_commit(&bars->dq_full[b]);
-        mma_commit(&bars->ds_free);
+          mma_ss(tmem + C::kColDQ, mnmaj(ds_s, kk), mnmaj(k_s, kk), kIdQ, kk > 0);
+        mma_commit(&bars->dq_full);
+        mma_commit(&bars->ds_free[b]);
         mma_commit(&bars->q_empty[st]);
-        if (t + 1 < n) issue_dp((t + 1) & 1);
       }
       __syncwarp();
+      if (++st == NS) st = 0;
     }
-    if (lane == 0) mma_commit(&bars->acc_done);
+    if (lane == 0) mma_commit(&bars->grad_done);
     __syncwarp();
-    // Nothing may be in flight on the tensor core when TMEM is released.
-    mbar_wait_warp(&bars->acc_done, 0, drain_wc);
+  }
+  teardown();
   } else if (warp >= kBwdDrainWarp0) {
     // ---------------------------------------------------------------- dQ drain
     const int qd = warp & 3;
@@ -375,23 +424,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     int t = 0;
     bool ok = true;
     for (; t < n; ++t) {
-      const int b = t & 1;
-      if (!(ok = mbar_wait_warp(&bars->dq_full[b], (t >> 1) & 1, wc))) break;
+      if (!(ok = mbar_wait_warp_inl(&bars->dq_full, t & 1, wc))) break;
+      FA_TRACE(20, t);
       tc_fence_after_sync();
-      uint32_t x[D];
-#pragma unroll
-      for (int h = 0; h < D / 32; ++h) tmem_ld32(tmem + lane_off + C::col_dq(b) + h * 32, x + h * 32);
-      tmem_ld_wait();
-#pragma unroll
-      for (int h = 0; h < D / 32; ++h) reg_fence32(x + h * 32);
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->dq_free[b]);
       float* dst = p.dq_acc + dq_acc_offset(bh, i0 + t, p.n_qt, 0, r, D);
+      // 32 columns at a time (the drain's register budget); the buffer is released once
+      // the last columns are in registers.
 #pragma unroll
-      for (int c4 = 0; c4 < D / 4; ++c4)
-        red_add_v4(dst + (size_t)c4 * 512, __uint_as_float(x[4 * c4]), __uint_as_float(x[4 * c4 + 1]),
-                   __uint_as_float(x[4 * c4 + 2]), __uint_as_float(x[4 * c4 + 3]));
+      for (int h = 0; h < D / 32; ++h) {
+        uint32_t x[32];
+        tmem_ld32(tmem + lane_off + C::kColDQ + h * 32, x);
+        tmem_ld_wait();
+        reg_fence32(x);
+        if (h == D / 32 - 1) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->dq_free);
+          FA_TRACE(21, t);
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4)
+          red_add_v4(dst + (size_t)(h * 8 + c4) * 512, __uint_as_float(x[4 * c4]),
+                     __uint_as_float(x[4 * c4 + 1]), __uint_as_float(x[4 * c4 + 2]),
+                     __uint_as_float(x[4 * c4 + 3]));
+      }
     }
     if (!ok) {
       // Abandoned tiles: poison their dQ rows so that the failure cannot go unseen.
@@ -401,21 +457,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int c4 = 0; c4 < D / 4; ++c4) red_add_v4(dst + (size_t)c4 * 512, nan, nan, nan, nan);
       }
     }
+    teardown();
   } else {
     // ---------------------------------------------------------------- compute (warps 0-7)
     const int g = warp >> 2;          // query half: columns 64g .. 64g+63 of each tile
     const int qd = warp & 3;
     const int r = qd * 32 + lane;     // key row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
-    const uint32_t p_box = sbase + C::kP + g * C::kBox;
-    const uint32_t ds_box = sbase + C::kDS + g * C::kBox;
     bool ok = true;
-    for (int t = 0; t < n && ok; ++t) {
-      const int st = t & 1;
+    for (int t = 0, st = 0, ph = 0; t < n && ok; ++t) {
       const int i = i0 + t;
       const float* vec = reinterpret_cast<const float*>(sm + C::kVec + st * 1024);
-      if (!(ok = mbar_wait_warp(&bars->q_full[st], (t >> 1) & 1, wc))) break;
-      if (!(ok = mbar_wait_warp(&bars->s_full, t & 1, wc))) break;
+      if (!(ok = mbar_wait_warp_inl(&bars->q_full[st], ph, wc))) break;
+      if (!(ok = mbar_wait_warp_inl(&bars->s_full, t & 1, wc))) break;
+      FA_TRACE(10, t);
       tc_fence_after_sync();
       uint32_t s[64];
       tmem_ld32(tmem + lane_off + C::kColS + g * 64, s);
@@ -423,6 +478,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld_wait();
       reg_fence32(s);
       reg_fence32(s + 32);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->s_free);
       // Pᵀ = exp2(S·scale·log2e − lse2_q), zero above the diagonal (key > query)
       float pr[64];
       const float4* l4 = reinterpret_cast<const float4*>(vec + g * 64);
@@ -439,16 +497,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int c = 0; c < 64; ++c)
           if (r > g * 64 + c) pr[c] = 0.f;
       }
-      if (t >= 1 && !(ok = mbar_wait_warp(&bars->p_free, (t - 1) & 1, wc))) break;
+      FA_TRACE(11, t);
+      if (t >= 1 && !(ok = mbar_wait_warp_inl(&bars->p_free, (t - 1) & 1, wc))) break;
+      FA_TRACE(12, t);
+      uint32_t pk[32];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) st_row_chunk_sw128(p_box, r, ch, pr + ch * 8);
-      fence_proxy_async_smem();
+      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+      tc_fence_after_sync();
+      tmem_st32(tmem + lane_off + C::kColP + g * 32, pk);
+      tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->p_full);
-      // dSᵀ = Pᵀ ∘ (dPᵀ − D_q)
-      if (!(ok = mbar_wait_warp(&bars->dp_full, t & 1, wc))) break;
-      if (t >= 1 && !(ok = mbar_wait_warp(&bars->ds_free, (t - 1) & 1, wc))) break;
+      FA_TRACE(13, t);
+      // dSᵀ = Pᵀ ∘ (dPᵀ − D_q), into shared-memory buffer t mod 2
+      const int b = t & 1;
+      const uint32_t ds_box = sbase + C::kDS + b * C::kDSBytes + g * C::kBox;
+      if (!(ok = mbar_wait_warp_inl(&bars->dp_full, t & 1, wc))) break;
+      FA_TRACE(14, t);
+      if (t >= 2 && !(ok = mbar_wait_warp_inl(&bars->ds_free[b], ((t >> 1) - 1) & 1, wc))) break;
+      FA_TRACE(15, t);
       tc_fence_after_sync();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -456,26 +524,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld32(tmem + lane_off + C::kColDP + g * 64 + h * 32, dp);
         tmem_ld_wait();
         reg_fence32(dp);
-        const float4* d4 = reinterpret_cast<const float4*>(vec + 128 + g * 64 + h * 32);
-        float ds[32];
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float4 dd = d4[c / 4];
-          ds[c] = pr[h * 32 + c] * (__uint_as_float(dp[c]) - dd.x);
-          ds[c + 1] = pr[h * 32 + c + 1] * (__uint_as_float(dp[c + 1]) - dd.y);
-          ds[c + 2] = pr[h * 32 + c + 2] * (__uint_as_float(dp[c + 2]) - dd.z);
-          ds[c + 3] = pr[h * 32 + c + 3] * (__uint_as_float(dp[c + 3]) - dd.w);
+        if (h == 1) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->dp_free);
         }
+        const float4* d4 = reinterpret_cast<const float4*>(vec + 128 + g * 64 + h * 32);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) st_row_chunk_sw128(ds_box, r, h * 4 + ch, ds + ch * 8);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 da = d4[2 * q4], db = d4[2 * q4 + 1];
+          const int c = h * 32 + q4 * 8;
+          const uint32_t* dq8 = dp + q4 * 8;
+          float ds[8];
+          ds[0] = pr[c] * (__uint_as_float(dq8[0]) - da.x);
+          ds[1] = pr[c + 1] * (__uint_as_float(dq8[1]) - da.y);
+          ds[2] = pr[c + 2] * (__uint_as_float(dq8[2]) - da.z);
+          ds[3] = pr[c + 3] * (__uint_as_float(dq8[3]) - da.w);
+          ds[4] = pr[c + 4] * (__uint_as_float(dq8[4]) - db.x);
+          ds[5] = pr[c + 5] * (__uint_as_float(dq8[5]) - db.y);
+          ds[6] = pr[c + 6] * (__uint_as_float(dq8[6]) - db.z);
+          ds[7] = pr[c + 7] * (__uint_as_float(dq8[7]) - db.w);
+          st_row_chunk_sw128(ds_box, r, h * 4 + q4, ds);
+        }
       }
       fence_proxy_async_smem();
-      tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->ds_full);
+      if (lane == 0) mbar_arrive(&bars->ds_full[b]);
+      FA_TRACE(16, t);
+      if (++st == NS) { st = 0; ph ^= 1; }
     }
     // ---- epilogue: warpgroup 0 writes dV_j, warpgroup 1 writes scale·dK_j
-    const bool done = ok && mbar_wait_warp(&bars->acc_done, 0, wc) && !bars->abort;
+    const bool done = ok && mbar_wait_warp_inl(&bars->grad_done, 0, wc) && !bars->abort;
     const int key = j * 128 + r;
     tc_fence_after_sync();
     uint32_t x[D];
@@ -503,13 +582,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         *reinterpret_cast<uint4*>(dst + c) = v;
       }
     }
-  }
-
-  tc_fence_before_sync();
-  __syncthreads();
-  if (warp == kBwdMmaWarp) {
-    tc_fence_after_sync();
-    tmem_dealloc(tmem, 512);
+    teardown();
   }
 }
 

@@ -125,6 +125,34 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, c
   return mbar_wait_warp_slow(bar, parity, w);
 }
 
+// The same wait with its slow path inlined (no call in the waiting loop).
+__device__ __forceinline__ bool mbar_wait_warp_inl(uint64_t* bar, uint32_t parity,
+                                                   const WaitCtl& w) {
+  if (__shfl_sync(0xffffffffu, mbar_try_wait(bar, parity) ? 1u : 0u, 0)) return true;
+#pragma unroll 1
+  for (int i = 0; i < 4096; ++i)
+    if (__shfl_sync(0xffffffffu, mbar_try_wait(bar, parity) ? 1u : 0u, 0)) return true;
+  uint64_t t0 = global_timer_ns();
+  t0 = __shfl_sync(0xffffffffu, t0, 0);
+#pragma unroll 1
+  for (uint32_t it = 1;; ++it) {
+    if (__shfl_sync(0xffffffffu, mbar_try_wait(bar, parity) ? 1u : 0u, 0)) return true;
+    if ((it & 63u) == 0u) {
+      uint32_t verdict = 0u;  // 1 = give up (another role aborted), 2 = timed out here
+      if ((threadIdx.x & 31u) == 0u) {
+        if (*w.abort) verdict = 1u;
+        else if (global_timer_ns() - t0 > w.timeout_ns) verdict = 2u;
+      }
+      verdict = __shfl_sync(0xffffffffu, verdict, 0);
+      if (verdict == 2u && (threadIdx.x & 31u) == 0u) {
+        *w.abort = 1u;
+        if (w.status) atomicExch(w.status, kErrTimeout);
+      }
+      if (verdict != 0u) return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------------
 // TMA (bulk tensor copies global -> shared, completion counted on an mbarrier)
 // ------------------------------------------------------------------------------------

@@ -179,3 +179,4 @@ def test_bwd_valid_call_without_device_reports_unsupported(lib):
 
 def test_bwd_flop_count():
     assert fa.bwd_flops(4, 12, 4096, 64, True) == 2.5 * fa.flops(4, 12, 4096, 64, True)
+
