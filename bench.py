@@ -11,6 +11,10 @@ inputs in pinned host memory and the host<->device copies inside the timed regio
 L2: each step touches ~0.8 GB of distinct inputs and outputs (more than 6× the 129 MB L2),
 so every launch reads inputs last touched a full step earlier.
 
+The same line carries a `backward` object: the gradient pass (dQ, dK, dV through fa_bwd)
+timed the same way over the same sweep, K steps, with an upstream gradient dO drawn per T;
+FLOPs are 2.5× the forward's (five T×T×d products instead of two).
+
 `--impl reference` times the fp64 CPU oracle (the plain definition, numpy) on this machine's
 host cores on a bounded sample of the same workload and prints the same JSON line.
 
@@ -39,6 +43,7 @@ B, H, D = 4, 12, 64
 SWEEP = (512, 1024, 2048, 4096, 8192, 16384)
 METRIC = "attn fwd TFLOP/s (bf16, B4 H12 d64, T 512\u201316k, causal) and % of tensor peak"
 WORKLOAD = "causal attention forward, bf16, B4 H12 d64, T sweep 512-16384 (one launch per T per step)"
+BWD_METRIC = "attn bwd TFLOP/s (bf16, B4 H12 d64, T 512\u201316k, causal; 2.5x forward FLOPs)"
 
 
 def _peaks():
@@ -116,28 +121,33 @@ class ClockSampler:
                 "power_w_max": pmax, "reasons": sorted(reasons)}
 
 
-def _kernel_source_sha256() -> str:
-    import glob
+# Source files that decide each pass's kernels and launch configuration.
+KERNEL_SOURCES = {
+    "fwd": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_api.cu"),
+    "bwd": ("sm103.cuh", "fa_bwd_kernel.cuh", "fa_bwd_d64.cu", "fa_bwd_api.cu"),
+}
+
+
+def kernel_source_sha256(which: str = "fwd") -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "exact_attention_23_gb300", "csrc", "*"))):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(os.path.basename(f).encode())
-            with open(f, "rb") as fh:
-                h.update(fh.read())
+    for name in KERNEL_SOURCES[which]:
+        h.update(name.encode())
+        with open(os.path.join(ROOT, "exact_attention_23_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()
 
 
-def _measured_traffic():
+def _measured_traffic(which: str = "fwd"):
     """DRAM bytes per launch of the dominant kernel from the committed ncu record, or None
     when the kernel sources changed after the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic_fa_fwd_d64_causal_t16384.json")
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_fa_{which}_d64_causal_t16384.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except Exception:
         return None
-    if rec.get("kernel_source_sha256") != _kernel_source_sha256():
+    if rec.get("kernel_source_sha256") != kernel_source_sha256(which):
         return None
     return float(rec["dram_bytes_per_launch"])
 
@@ -215,6 +225,31 @@ def _oracle_sample(budget_s: float):
     desc = (f"{rows_per_T} query rows per T (evenly spaced, causal) of one head at each T in "
             f"{list(SWEEP)}, d=64, repeated {passes}x; FLOPs counted as 4·(i+1)·d per row i")
     return flops, dt, desc
+
+
+def _oracle_bwd_sample(budget_s: float):
+    """Time the fp64 oracle's full backward of one head at the two shortest lengths of the
+    sweep; returns (algorithmic FLOPs, seconds, description)."""
+    import oracle
+    from exact_attention_23_gb300 import inputs
+    import exact_attention_23_gb300 as fa
+    work = []
+    for T in SWEEP[:2]:
+        q, k, v = inputs.make_qkv(1, 1, T, D, seed=3 + SWEEP.index(T))
+        do = inputs.make_do(1, 1, T, D, seed=3 + SWEEP.index(T))
+        work.append((T, *(inputs.to_f64_numpy(t[0, 0]) for t in (q, k, v, do))))
+    flops, passes = 0.0, 0
+    t0 = time.perf_counter()
+    while True:
+        for T, q, k, v, do in work:
+            oracle.attention_backward_head(q, k, v, do, True, D ** -0.5)
+            flops += fa.bwd_flops(1, 1, T, D, True)
+        passes += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return flops, dt, (f"full backward of one head at T in {list(SWEEP[:2])}, d=64, causal, "
+                       f"repeated {passes}x; algorithmic FLOPs (2.5x the causal forward's)")
 
 
 def _cores() -> int:
@@ -327,6 +362,59 @@ def run_gpu(args):
                       "gbs": by / ms / 1e6, "frac_hbm": by / ms / 1e6 / hbm_peak})
     dom = max(per_T, key=lambda r: fa.flops(B, H, r["T"], D, True))
 
+    # ---- backward: the same sweep, K steps, dO drawn per T, workspace allocated up front
+    bsets = []
+    for j, s in enumerate(sets):
+        T, _, _, _, qd, kd, vd, o, lse = s
+        dod = inputs.make_do(B, H, T, D, seed=3 + SWEEP.index(T) if T in SWEEP else 100 + T).to(dev)
+        grads = tuple(torch.empty_like(qd) for _ in range(3))
+        ws_t = fa.bwd_workspace(B, H, T, D, device=dev)
+        bsets.append((T, qd, kd, vd, o, lse, dod, grads, ws_t))
+
+    def launch_bwd(bs):
+        T, qd, kd, vd, o, lse, dod, (dq, dk, dv), ws_t = bs
+        rc = fa.fa_bwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), dod.data_ptr(),
+                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                       ws_t.data_ptr(), ws_t.numel(), B, H, T, D, 1, scale, stream.cuda_stream)
+        if rc != fa.FA_OK:
+            raise fa.FAError(rc, "fa_bwd")
+
+    for _ in range(args.warmup):
+        for bs in bsets:
+            launch_bwd(bs)
+    torch.cuda.synchronize(dev)
+    bev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in bsets] for _ in range(args.steps)]
+    b_start = torch.cuda.Event(enable_timing=True)
+    b_end = torch.cuda.Event(enable_timing=True)
+    bsampler = ClockSampler(_smi_index(dev.index))
+    bsampler.start()
+    time.sleep(0.3)
+    _barrier(ws)
+    torch.cuda.synchronize(dev)
+    b_start.record(stream)
+    for it in range(args.steps):
+        for j, bs in enumerate(bsets):
+            bev[it][j][0].record(stream)
+            launch_bwd(bs)
+            bev[it][j][1].record(stream)
+    b_end.record(stream)
+    torch.cuda.synchronize(dev)
+    _barrier(ws)
+    bclocks = bsampler.stop()
+    bflops_step = sum(fa.bwd_flops(B, H, T, D, True) for T in sweep)
+    bvalue, b_ms = aggregate_tflops(bflops_step, args.steps, b_start.elapsed_time(b_end), ws)
+    bper_T = []
+    for j, bs in enumerate(bsets):
+        T = bs[0]
+        ms = statistics.mean(bev[it][j][0].elapsed_time(bev[it][j][1]) for it in range(args.steps))
+        fl = fa.bwd_flops(B, H, T, D, True)
+        bper_T.append({"T": T, "ms": ms, "tflops": fl / ms / 1e9,
+                       "frac_of_sustained": fl / ms / 1e9 / bf16_sus})
+    bdom = max(bper_T, key=lambda r: r["T"])
+    launches += 3 * args.steps * len(bsets)
+    del bsets
+
     # ---- end to end: pinned host inputs -> device -> forward -> host, per step
     e2e_steps = max(1, min(args.steps, 10))
     pinned = []
@@ -363,6 +451,11 @@ def run_gpu(args):
             fl, dt, desc = _oracle_sample(args.cpu_seconds)
             cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
                    "sample": desc + "; numpy/BLAS default threads"}
+        bcpu = None
+        if ws == 1 and not args.no_cpu_baseline:
+            fl, dt, desc = _oracle_bwd_sample(max(1.0, args.cpu_seconds / 3))
+            bcpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+                    "sample": desc + "; numpy/BLAS default threads"}
         result = {
             "metric": METRIC,
             "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
@@ -389,6 +482,22 @@ def run_gpu(args):
             "gpu_launches": launches,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "backward": {
+                "metric": BWD_METRIC, "value": bvalue, "unit": "TFLOP/s",
+                "ms_per_step": b_ms / args.steps, "steps": args.steps,
+                "frac_of_peak": {"sustained": bvalue / ws / bf16_sus, "peak_kind": peak_kind},
+                "per_T": bper_T,
+                "roofline": {"bound": "tensor", "achieved": bdom["tflops"], "peak": bf16_sus,
+                             "unit": "TFLOP/s", "frac": bdom["tflops"] / bf16_sus,
+                             "traffic": _measured_traffic("bwd") if bdom["T"] == 16384 else None,
+                             "kernel": f"fa_bwd_main_kernel<64,causal> at T={bdom['T']}; achieved "
+                                       f"over the whole fa_bwd call (prep + main + dQ conversion), "
+                                       f"{fa.bwd_flops(B, H, bdom['T'], D, True):.4g} FLOP; peak = "
+                                       f"{peak_kind} sustained bf16"},
+                "gpu_launches": 3 * args.steps * len(sweep),
+                "clocks": bclocks,
+                "cpu_baseline": bcpu,
+            },
         }
         print(json.dumps(result), flush=True)
     if ws > 1:

@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfa.so")
 
-SOURCES = ["fa_api.cu", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_bwd_d64.cu", "fa_noalloc.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_bwd_d64.cu", "fa_bwd_api.cu",
+           "fa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I", INCLUDE, "-I", CSRC]
@@ -51,7 +52,9 @@ def build(verbose: bool = False) -> str:
     with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
         f.write(log)
     tmp = LIB + ".tmp"
-    cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
+    cmd = [nvcc(), *ARCH, "-shared", "-Xlinker",
+           "--version-script=" + os.path.join(CSRC, "exports.map"), "-o", tmp,
+           *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

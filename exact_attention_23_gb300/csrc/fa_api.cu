@@ -1,5 +1,6 @@
-// Host side of the C ABI declared in include/fa.h: argument validation, tensor-map
-// encoding for the TMA loads, and the launch on the caller's stream.
+// Host side of the C ABI declared in include/fa.h, forward pass and shared helpers:
+// argument validation, tensor-map encoding for the TMA loads, and the launch on the
+// caller's stream. The backward's entry points are in fa_bwd_api.cu.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -10,14 +11,11 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_host.h"
 #include "fa_launch.h"
 
-namespace {
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+namespace fa {
+namespace host {
 
 // The driver's tensor-map encoder, looked up once through the runtime (no link-time
 // dependency on libcuda).
@@ -37,9 +35,9 @@ EncodeTiledFn encode_fn() {
 
 using fa::kMaxDevices;
 // 0 = unknown, 1 = supported (cc 10.3), 2 = unsupported
-int g_dev_state[kMaxDevices];
-int g_dev_sms[kMaxDevices];
-std::mutex g_dev_mu;
+static int g_dev_state[kMaxDevices];
+static int g_dev_sms[kMaxDevices];
+static std::mutex g_dev_mu;
 
 int check_device(int* dev_out, int* sms_out) {
   int dev = -1;
@@ -92,7 +90,10 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0u; }
 
-}  // namespace
+}  // namespace host
+}  // namespace fa
+
+using namespace fa::host;
 
 extern "C" {
 
@@ -180,107 +181,6 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T,
            int d, int causal, float scale, void* stream) {
   return fa_fwd_ex(q, k, v, o, lse, B, H, T, d, causal, scale, nullptr, 0ull, 0u, stream);
-}
-
-// ---------------------------------------------------------------------------- backward
-
-// Workspace: [BH][T_pad] fp32 lse2, [BH][T_pad] fp32 D, [BH][T_pad][d] fp32 dQ accumulator,
-// each section starting on a 256-byte boundary. Returns 0 for unsupported sizes.
-size_t fa_bwd_workspace_size(int B, int H, int T, int d) {
-  if (B <= 0 || H <= 0 || T <= 0 || d != 64) return 0;
-  const long long BH = static_cast<long long>(B) * H;
-  const long long T_pad = (static_cast<long long>(T) + 127) / 128 * 128;
-  if (BH > INT32_MAX || T_pad > INT32_MAX || (T_pad / 128) * BH > INT32_MAX) return 0;
-  auto up = [](unsigned long long x) { return (x + 255ull) / 256ull * 256ull; };
-  const unsigned long long rows = static_cast<unsigned long long>(BH) * T_pad;
-  if (rows > (1ull << 56) / (static_cast<unsigned long long>(d) + 2) / 4) return 0;
-  return static_cast<size_t>(2 * up(rows * 4) + up(rows * d * 4));
-}
-
-int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
-              const float* lse, void* dq, void* dk, void* dv, void* workspace,
-              size_t workspace_bytes, int B, int H, int T, int d, int causal, float scale,
-              int* status, unsigned long long timeout_ns, unsigned int flags, void* stream) {
-  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
-    return FA_ERR_INVALID_ARG;
-  if (B <= 0 || H <= 0 || T <= 0 || d != 64) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
-  if ((flags & ~static_cast<unsigned>(FA_FLAG_TEST_STARVE_Q)) != 0u) return FA_ERR_INVALID_ARG;
-  const size_t need = fa_bwd_workspace_size(B, H, T, d);
-  if (need == 0 || workspace_bytes < need) return FA_ERR_INVALID_ARG;
-  const long long BH = static_cast<long long>(B) * H;
-  const long long n_qt = (static_cast<long long>(T) + 127) / 128;
-  const long long T_pad = n_qt * 128;
-  const long long elems = BH * T * d;
-  if (elems >= (1LL << 62) / 2) return FA_ERR_INVALID_ARG;
-  if (static_cast<long long>(T) * d * 2 >= (1LL << 40)) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
-      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0u)
-    return FA_ERR_MISALIGNED;
-  // Outputs and workspace must not overlap any input or one another.
-  const size_t tb = static_cast<size_t>(elems) * 2, lb = static_cast<size_t>(BH) * T * 4;
-  const void* ins[6] = {q, k, v, o, dout, lse};
-  const size_t in_bytes[6] = {tb, tb, tb, tb, tb, lb};
-  const void* outs[4] = {dq, dk, dv, workspace};
-  const size_t out_bytes[4] = {tb, tb, tb, need};
-  for (int a = 0; a < 4; ++a) {
-    for (int b = 0; b < 6; ++b)
-      if (overlaps(outs[a], out_bytes[a], ins[b], in_bytes[b])) return FA_ERR_INVALID_ARG;
-    for (int b = a + 1; b < 4; ++b)
-      if (overlaps(outs[a], out_bytes[a], outs[b], out_bytes[b])) return FA_ERR_INVALID_ARG;
-  }
-
-  int dev = -1, sms = 0;
-  const int dst = check_device(&dev, &sms);
-  if (dst != FA_OK) return dst;
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return FA_ERR_LAUNCH;
-
-  fa::BwdLaunch a;
-  if (!encode_map(enc, &a.tm_q, q, T, d, static_cast<int>(BH)) ||
-      !encode_map(enc, &a.tm_k, k, T, d, static_cast<int>(BH)) ||
-      !encode_map(enc, &a.tm_v, v, T, d, static_cast<int>(BH)) ||
-      !encode_map(enc, &a.tm_do, dout, T, d, static_cast<int>(BH)))
-    return FA_ERR_INVALID_ARG;
-  auto up = [](size_t x) { return (x + 255u) / 256u * 256u; };
-  const size_t rows = static_cast<size_t>(BH) * static_cast<size_t>(T_pad);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  a.lse2 = reinterpret_cast<float*>(ws);
-  a.dvec = reinterpret_cast<float*>(ws + up(rows * 4));
-  a.p.dq_acc = reinterpret_cast<float*>(ws + 2 * up(rows * 4));
-  a.p.lse2 = a.lse2;
-  a.p.dvec = a.dvec;
-  a.p.dk = static_cast<__nv_bfloat16*>(dk);
-  a.p.dv = static_cast<__nv_bfloat16*>(dv);
-  a.p.status = status;
-  a.p.T = T;
-  a.p.T_pad = static_cast<int>(T_pad);
-  a.p.BH = static_cast<int>(BH);
-  a.p.n_qt = static_cast<int>(n_qt);
-  a.p.scale = scale;
-  a.p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-  a.p.timeout_ns = timeout_ns ? timeout_ns : 2000000000ull;
-  a.p.flags = flags;
-  a.o = static_cast<const __nv_bfloat16*>(o);
-  a.dout = static_cast<const __nv_bfloat16*>(dout);
-  a.lse = lse;
-  a.dq = static_cast<__nv_bfloat16*>(dq);
-  a.grid_main = static_cast<unsigned>(n_qt * BH);
-  // The two streaming kernels: a few resident blocks per SM, grid-stride loops.
-  a.grid_prep = static_cast<unsigned>(sms) * 8u;
-  a.grid_dq = static_cast<unsigned>(sms) * 8u;
-  a.stream = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = fa::launch_bwd_d64(a, causal != 0);
-  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
-}
-
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-           const float* lse, void* dq, void* dk, void* dv, void* workspace,
-           size_t workspace_bytes, int B, int H, int T, int d, int causal, float scale,
-           void* stream) {
-  return fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, T, d,
-                   causal, scale, nullptr, 0ull, 0u, stream);
 }
 
 }  // extern "C"

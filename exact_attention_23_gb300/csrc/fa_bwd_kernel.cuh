@@ -110,6 +110,7 @@ struct BwdParams {
   int T_pad;           // n_qt · 128
   int BH;
   int n_qt;            // ceil(T / 128): query tiles = key tiles
+  int head_group;      // heads whose units are interleaved (see the unit order)
   float scale;
   float scale_log2;    // scale · log2(e)
   uint64_t timeout_ns;
@@ -227,9 +228,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   BwdBars* bars = reinterpret_cast<BwdBars*>(sm + C::kBar);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // Heaviest units first: under the causal mask key tile j sees n_qt − j query tiles.
-  const int j = blockIdx.x / p.BH;
-  const int bh = blockIdx.x % p.BH;
+  // Unit order: heads in groups of head_group, small enough that a group's Q, dO and dQ
+  // accumulator stay in L2 while its CTAs run; within a group, heaviest units first (under
+  // the causal mask key tile j sees n_qt − j query tiles), all heads at one j together.
+  const int per_group = p.head_group * p.n_qt;
+  const int grp = blockIdx.x / per_group;
+  const int within = blockIdx.x - grp * per_group;
+  const int gsize = min(p.head_group, p.BH - grp * p.head_group);
+  const int j = within / gsize;
+  const int bh = grp * p.head_group + within % gsize;
   const int i0 = CAUSAL ? j : 0;
   const int n = p.n_qt - i0;
 

@@ -1,0 +1,27 @@
+// Host-side helpers shared by the forward (fa_api.cu) and backward (fa_bwd_api.cu) entry
+// points. Internal; not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace fa {
+namespace host {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder (looked up once), or null.
+EncodeTiledFn encode_fn();
+// FA_OK with the current device and its SM count if it is compute capability 10.3.
+int check_device(int* dev_out, int* sms_out);
+// 3-D map over a [B·H][T][d] bf16 tensor, boxes of 64 columns × 128 rows × 1 head.
+bool encode_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, int T, int d, int BH);
+bool overlaps(const void* a, size_t na, const void* b, size_t nb);
+bool aligned16(const void* p);
+
+}  // namespace host
+}  // namespace fa

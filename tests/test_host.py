@@ -180,3 +180,18 @@ def test_bwd_valid_call_without_device_reports_unsupported(lib):
 def test_bwd_flop_count():
     assert fa.bwd_flops(4, 12, 4096, 64, True) == 2.5 * fa.flops(4, 12, 4096, 64, True)
 
+
+
+def test_library_exports_only_the_c_abi(lib):
+    """libfa.so exports exactly the functions include/fa.h declares (a linker version
+    script hides everything else)."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", _binding.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    funcs = sorted(line.split()[-1] for line in out.splitlines()
+                   if len(line.split()) == 3 and line.split()[1] == "T")
+    assert funcs == _header_functions()
