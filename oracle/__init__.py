@@ -22,7 +22,11 @@ from .naive import (  # noqa: F401
     attention_backward_head,
     attention_backward_magnitudes,
     attention_backward_rows,
+    attention_general,
+    attention_general_head,
     attention_rows,
+    general_mask,
+    merge_partials,
     online_softmax_trace,
     online_weighted_sum,
     safe_softmax,

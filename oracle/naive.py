@@ -349,3 +349,81 @@ def attention_backward_magnitudes(q, k, v, do, causal: bool, scale: float,
                 mq[b, h, rows] = scale * (a @ np.abs(k[b, h]))
                 mk[b, h] += scale * (a.T @ np.abs(q[b, h, rows]))
     return mq, mk, mv
+
+
+# --------------------------------------------------------------------------------------
+# General form: Tq queries over Tk keys, bottom-right causal alignment, block masks, and
+# the merge of results computed over disjoint key ranges.
+# --------------------------------------------------------------------------------------
+
+def general_mask(Tq: int, Tk: int, causal: bool, block_mask=None, block: int = 128):
+    """Boolean [Tq, Tk] visibility. Causal is aligned bottom-right: query i sees key j iff
+    j ≤ i + (Tk − Tq) (the last query sees every key, as a new token does against its KV
+    cache — [HW-FA] step ①'s note that generation keeps the K/V of all earlier tokens).
+    block_mask ([ceil(Tq/block), ceil(Tk/block)], nonzero = keep) switches whole blocks
+    off, the tile-skipping generalisation of causal masking in [KCS] "块稀疏注意力 V2 和 V3"."""
+    vis = np.ones((Tq, Tk), dtype=bool)
+    if causal:
+        vis &= np.arange(Tk)[None, :] <= (np.arange(Tq) + (Tk - Tq))[:, None]
+    if block_mask is not None:
+        bm = np.asarray(block_mask) != 0
+        vis &= bm[np.arange(Tq) // block][:, np.arange(Tk) // block]
+    return vis
+
+
+def attention_general_head(q, k, v, causal: bool, scale: float, block_mask=None,
+                           block: int = 128):
+    """(O, LSE) of one head for q [Tq, d], k and v [Tk, d] under general_mask. A row that
+    sees no key at all has O = 0 and LSE = −∞ (the softmax over an empty set is undefined;
+    this is the convention of the library)."""
+    q = _as_f64(q)
+    k = _as_f64(k)
+    v = _as_f64(v)
+    Tq, Tk = q.shape[0], k.shape[0]
+    vis = general_mask(Tq, Tk, causal, block_mask, block)
+    o = np.zeros((Tq, v.shape[1]))
+    lse = np.full(Tq, -np.inf)
+    for r0 in range(0, Tq, _ROW_CHUNK):
+        rows = np.arange(r0, min(Tq, r0 + _ROW_CHUNK))
+        s = scores(q[rows], k, scale)
+        s = np.where(vis[rows], s, -np.inf)
+        live = vis[rows].any(axis=1)
+        if live.any():
+            p, m, l = safe_softmax(s[live])
+            o[rows[live]] = weighted_values(p, v)
+            lse[rows[live]] = logsumexp_from(m, l)
+    return o, lse
+
+
+def attention_general(q, k, v, causal: bool, scale: float, block_mask=None, block: int = 128):
+    """[B, H, Tq, d] queries over [B, H, Tk, d] keys/values. block_mask is None, one
+    [n_qb, n_kb] array shared by every head, or [B·H, n_qb, n_kb] per head."""
+    q = _as_f64(q)
+    B, H, Tq, d = q.shape
+    o = np.empty((B, H, Tq, v.shape[-1]))
+    lse = np.empty((B, H, Tq))
+    for b in range(B):
+        for h in range(H):
+            bm = None
+            if block_mask is not None:
+                bm = np.asarray(block_mask)
+                bm = bm[b * H + h] if bm.ndim == 3 else bm
+            o[b, h], lse[b, h] = attention_general_head(q[b, h], k[b, h], v[b, h], causal,
+                                                        scale, bm, block)
+    return o, lse
+
+
+def merge_partials(o_parts, lse_parts):
+    """Combine results computed over disjoint key ranges (index 0 of each array = range):
+    with M = max_s LSE_s, weights w_s = exp(LSE_s − M), O = Σ w_s·O_s / Σ w_s and
+    LSE = M + ln Σ w_s. This is the merge [HW-FA] step ③ says the first version's outer
+    loop over K/V blocks needed; ranges that saw no key carry LSE = −∞ and weight 0."""
+    o_parts = _as_f64(o_parts)
+    lse_parts = _as_f64(lse_parts)
+    m = np.max(lse_parts, axis=0)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    w = np.exp(lse_parts - m_safe[None])
+    wsum = np.sum(w, axis=0)
+    o = np.sum(w[..., None] * o_parts, axis=0) / np.where(wsum > 0, wsum, 1.0)[..., None]
+    lse = np.where(wsum > 0, m_safe + np.log(np.where(wsum > 0, wsum, 1.0)), -np.inf)
+    return o, lse

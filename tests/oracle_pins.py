@@ -393,10 +393,130 @@ def pin_bwd_magnitudes(orc):
         assert np.max(np.abs(mv - dv)) <= 1e-12
 
 
+# ------------------------------------------------------------- general form (Tq ≠ Tk, masks)
+
+def brute_force_general(q, k, v, causal, scale, block_mask, block):
+    """Pure-Python loops: query i sees key j iff (not causal or j ≤ i + Tk − Tq) and the
+    block (i // block, j // block) is on; a row that sees nothing gives O = 0, LSE = −∞."""
+    q = np.asarray(q).tolist()
+    k = np.asarray(k).tolist()
+    v = np.asarray(v).tolist()
+    Tq, Tk, d = len(q), len(k), len(q[0])
+    o = [[0.0] * d for _ in range(Tq)]
+    lse = [-math.inf] * Tq
+    for i in range(Tq):
+        keys = [j for j in range(Tk)
+                if (not causal or j <= i + Tk - Tq)
+                and (block_mask is None or block_mask[i // block][j // block])]
+        if not keys:
+            continue
+        s = {j: scale * sum(q[i][t] * k[j][t] for t in range(d)) for j in keys}
+        m = max(s.values())
+        e = {j: math.exp(s[j] - m) for j in keys}
+        l = sum(e.values())
+        for t in range(d):
+            o[i][t] = sum(e[j] * v[j][t] for j in keys) / l
+        lse[i] = m + math.log(l)
+    return np.array(o), np.array(lse)
+
+
+def pin_general_bruteforce(orc):
+    """Tq ≠ Tk, bottom-right causal, random block masks (block = 2 rows/keys) including
+    empty block rows: numpy general form == pure-Python loops within 1e-12."""
+    r = _rng(40)
+    for n, (Tq, Tk, causal) in enumerate([(3, 7, True), (5, 5, True), (4, 9, False), (1, 6, True),
+                                          (7, 3, False), (6, 6, False)]):
+        q = r.standard_normal((Tq, 3))
+        k = r.standard_normal((Tk, 3))
+        v = r.standard_normal((Tk, 3))
+        for trial in range(3):
+            bm = None if trial == 0 else (r.random(((Tq + 1) // 2, (Tk + 1) // 2)) < 0.6)
+            if trial == 2:
+                bm[0, :] = False   # an empty row block
+            o, lse = orc.attention_general_head(q, k, v, causal, 0.8, bm, block=2)
+            ob, lb = brute_force_general(q, k, v, causal, 0.8, bm, 2)
+            assert np.max(np.abs(o - ob)) <= 1e-12, (n, trial)
+            fin = np.isfinite(lb)
+            assert np.array_equal(np.isneginf(lse), np.isneginf(lb)), (n, trial)
+            assert np.all(np.abs(lse[fin] - lb[fin]) <= 1e-12), (n, trial)
+
+
+def pin_general_reduces_to_attention(orc):
+    """Tq = Tk with no block mask (or an all-ones one) is plain attention; a block mask
+    that keeps exactly the blocks on or below the diagonal changes nothing under causal."""
+    q, k, v = _qkv(41, 1, 2, 300, 8)
+    for causal in (False, True):
+        o, lse = orc.attention(q, k, v, causal, 0.3)
+        og, lg = orc.attention_general(q, k, v, causal, 0.3)
+        assert np.max(np.abs(o - og)) <= 1e-13 and np.max(np.abs(lse - lg)) <= 1e-13
+        ones = np.ones((3, 3), dtype=np.uint8)
+        og, lg = orc.attention_general(q, k, v, causal, 0.3, ones)
+        assert np.max(np.abs(o - og)) <= 1e-13 and np.max(np.abs(lse - lg)) <= 1e-13
+    tri = np.tril(np.ones((3, 3), dtype=np.uint8))
+    o, lse = orc.attention(q, k, v, True, 0.3)
+    og, lg = orc.attention_general(q, k, v, True, 0.3, tri)
+    assert np.max(np.abs(o - og)) <= 1e-13 and np.max(np.abs(lse - lg)) <= 1e-13
+
+
+def pin_general_decode(orc):
+    """One query against Tk keys under causal (bottom-right) sees every key: it equals the
+    last row of full causal attention over the same keys, and with q = 0 the mean of V with
+    LSE = ln Tk. The causal rows of Tq < Tk equal the last Tq rows of full causal attention."""
+    _, k, v = _qkv(42, 1, 1, 37, 5)
+    q = _rng(43).standard_normal((1, 1, 1, 5))
+    full_q = np.concatenate([_rng(44).standard_normal((1, 1, 36, 5)), q], axis=2)
+    o_full, l_full = orc.attention(full_q, k, v, True, 0.6)
+    o, lse = orc.attention_general(q, k, v, True, 0.6)
+    assert np.max(np.abs(o[0, 0, 0] - o_full[0, 0, -1])) <= 1e-13
+    assert abs(lse[0, 0, 0] - l_full[0, 0, -1]) <= 1e-13
+    o, lse = orc.attention_general(np.zeros((1, 1, 1, 5)), k, v, True, 0.6)
+    assert np.max(np.abs(o[0, 0, 0] - v[0, 0].mean(axis=0))) <= 1e-13
+    assert abs(lse[0, 0, 0] - math.log(37)) <= 1e-13
+    o, lse = orc.attention_general(full_q[:, :, -9:], k, v, True, 0.6)
+    assert np.max(np.abs(o - o_full[:, :, -9:])) <= 1e-13
+    assert np.max(np.abs(lse - l_full[:, :, -9:])) <= 1e-13
+
+
+def pin_general_empty_rows(orc):
+    """A row block switched off entirely gives O = 0 and LSE = −∞ on exactly its rows."""
+    q, k, v = _qkv(45, 1, 1, 40, 4)
+    bm = np.ones((5, 5), dtype=np.uint8)
+    bm[2, :] = 0
+    o, lse = orc.attention_general(q, k, v, False, 0.5, bm, block=8)
+    assert np.all(o[0, 0, 16:24] == 0.0) and np.all(np.isneginf(lse[0, 0, 16:24]))
+    assert np.all(np.isfinite(lse[0, 0, :16])) and np.all(np.isfinite(lse[0, 0, 24:]))
+
+
+def pin_merge_partials(orc):
+    """Merging results over disjoint key ranges gives the full result: worked by hand for
+    two parts (O = 1, LSE = ln 1 and O = 2, LSE = ln 3 → O = 7/4, LSE = ln 4), and on data
+    with the key range split into 3 block ranges by block masks, causal and not, with one
+    range that some rows never see (LSE = −∞, weight 0)."""
+    o, lse = orc.merge_partials(np.array([[1.0], [2.0]]), np.array([0.0, math.log(3.0)]))
+    assert abs(o[0] - 1.75) <= 1e-15 and abs(lse - math.log(4.0)) <= 1e-15
+    q, k, v = _qkv(46, 1, 2, 24, 4)
+    for causal in (False, True):
+        o_full, l_full = orc.attention_general(q, k, v, causal, 0.7, None, block=8)
+        parts_o, parts_l = [], []
+        for s in range(3):
+            bm = np.zeros((3, 3), dtype=np.uint8)
+            bm[:, s] = 1
+            po, pl = orc.attention_general(q, k, v, causal, 0.7, bm, block=8)
+            parts_o.append(po)
+            parts_l.append(pl)
+        o, lse = orc.merge_partials(np.stack(parts_o), np.stack(parts_l))
+        assert np.max(np.abs(o - o_full)) <= 1e-13 and np.max(np.abs(lse - l_full)) <= 1e-13
+    # huge LSEs: the max shift keeps the merge finite
+    o, lse = orc.merge_partials(np.array([[1.0], [3.0]]), np.array([900.0, 900.0]))
+    assert abs(o[0] - 2.0) <= 1e-15 and abs(lse - (900.0 + math.log(2.0))) <= 1e-12
+
+
 ORACLE_PINS = [pin_bruteforce, pin_hand_example, pin_row_sums, pin_constant_v,
                pin_causal_row0, pin_uniform, pin_shift, pin_permutation, pin_large_scores,
                pin_rows_match_full, pin_sdpa_library]
 RECURRENCE_PINS = [pin_online_trace, pin_online_weighted_sum]
+GENERAL_PINS = [pin_general_bruteforce, pin_general_reduces_to_attention, pin_general_decode,
+                pin_general_empty_rows, pin_merge_partials]
 BACKWARD_PINS = [pin_bwd_finite_diff, pin_bwd_hand_example, pin_bwd_invariants,
                  pin_bwd_autograd, pin_bwd_sampled, pin_bwd_magnitudes]
 
@@ -418,4 +538,4 @@ def run_all(orc, pins):
     return failed
 
 
-__all__ = ["ORACLE_PINS", "RECURRENCE_PINS", "BACKWARD_PINS", "run_all", "brute_force", "load_page_facts"]
+__all__ = ["ORACLE_PINS", "RECURRENCE_PINS", "BACKWARD_PINS", "GENERAL_PINS", "run_all", "brute_force", "load_page_facts"]

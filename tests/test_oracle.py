@@ -11,7 +11,7 @@ import oracle.naive as oa
 from tests import oracle_pins as pins
 
 
-ALL_PINS = pins.ORACLE_PINS + pins.RECURRENCE_PINS + pins.BACKWARD_PINS
+ALL_PINS = pins.ORACLE_PINS + pins.RECURRENCE_PINS + pins.BACKWARD_PINS + pins.GENERAL_PINS
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
@@ -32,7 +32,8 @@ def test_page_facts_are_consistent():
 
 def test_oracle_package_exports():
     for name in ("attention", "attention_rows", "online_softmax_trace", "online_weighted_sum",
-                 "attention_backward", "attention_backward_rows", "attention_backward_cols"):
+                 "attention_backward", "attention_backward_rows", "attention_backward_cols",
+                 "attention_general", "merge_partials"):
         assert callable(getattr(oracle, name))
 
 
@@ -140,6 +141,37 @@ def _dv_unnormalised(p, do_rows):
     return (p / p.max(axis=1, keepdims=True)).T @ do_rows
 
 
+def _general_mask_top_left(Tq, Tk, causal, block_mask=None, block=128):
+    vis = np.ones((Tq, Tk), dtype=bool)
+    if causal:
+        vis &= np.arange(Tk)[None, :] <= np.arange(Tq)[:, None]
+    if block_mask is not None:
+        bm = np.asarray(block_mask) != 0
+        vis &= bm[np.arange(Tq) // block][:, np.arange(Tk) // block]
+    return vis
+
+
+def _general_mask_blocks_transposed(Tq, Tk, causal, block_mask=None, block=128):
+    vis = np.ones((Tq, Tk), dtype=bool)
+    if causal:
+        vis &= np.arange(Tk)[None, :] <= (np.arange(Tq) + (Tk - Tq))[:, None]
+    if block_mask is not None:
+        bm = (np.asarray(block_mask) != 0).T  # block (j, i) looked up for query i, key j
+        vis &= bm[np.arange(Tq) // block][:, np.arange(Tk) // block]
+    return vis
+
+
+def _merge_plain_average(o_parts, lse_parts):
+    o_parts = np.asarray(o_parts, float)
+    return o_parts.mean(axis=0), np.log(np.exp(np.asarray(lse_parts, float)).sum(axis=0))
+
+
+def _merge_no_shift(o_parts, lse_parts):
+    w = np.exp(np.asarray(lse_parts, float))
+    o = (w[..., None] * np.asarray(o_parts, float)).sum(axis=0) / w.sum(axis=0)[..., None]
+    return o, np.log(w.sum(axis=0))
+
+
 MUTANTS = {
     "scores:no_scale": ("scores", _no_scale),
     "mask:wrong_direction": ("apply_causal_mask", _mask_wrong_way),
@@ -153,6 +185,13 @@ MUTANTS = {
     "lse:without_max": ("logsumexp_from", _lse_without_max),
     "trace:no_rescale": ("online_softmax_trace", _trace_no_rescale),
     "weighted:no_acc_rescale": ("online_weighted_sum", _weighted_no_acc_rescale),
+}
+
+GENERAL_MUTANTS = {
+    "general:top_left_causal": ("general_mask", _general_mask_top_left),
+    "general:block_mask_transposed": ("general_mask", _general_mask_blocks_transposed),
+    "merge:plain_average": ("merge_partials", _merge_plain_average),
+    "merge:no_max_shift": ("merge_partials", _merge_no_shift),
 }
 
 BACKWARD_MUTANTS = {
@@ -172,6 +211,14 @@ def test_pins_catch_planted_mistake(name, monkeypatch):
     monkeypatch.setattr(oa, attr, broken)
     failed = pins.run_all(oa, pins.ORACLE_PINS + pins.RECURRENCE_PINS)
     assert failed, f"no pin caught the planted mistake {name}"
+
+
+@pytest.mark.parametrize("name", sorted(GENERAL_MUTANTS))
+def test_general_pins_catch_planted_mistake(name, monkeypatch):
+    attr, broken = GENERAL_MUTANTS[name]
+    monkeypatch.setattr(oa, attr, broken)
+    failed = pins.run_all(oa, pins.GENERAL_PINS)
+    assert failed, f"no general-form pin caught the planted mistake {name}"
 
 
 @pytest.mark.parametrize("name", sorted(BACKWARD_MUTANTS))
