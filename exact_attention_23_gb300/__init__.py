@@ -2,8 +2,10 @@
 
 ``fwd(q, k, v, causal)`` returns ``(o, lse)`` for contiguous bf16 CUDA tensors of shape
 [B, H, T, d] (d = 64 or 128): o = softmax(scale·QKᵀ [+causal mask])·V in bf16 and the
-per-row natural-log logsumexp in fp32. ``bwd(q, k, v, o, lse, do, causal)`` returns the
-gradients (dq, dk, dv) for d = 64. The work is done by the CUDA kernels of ``libfa.so``
+per-row natural-log logsumexp in fp32. ``fwd_kv`` attends Tq queries to Tk ≥ Tq keys
+(bottom-right causal; key range split over CTAs when that fills the GPU), and
+``fwd_block_sparse`` skips 128×128 blocks switched off by a block mask.
+``bwd(q, k, v, o, lse, do, causal)`` returns the gradients (dq, dk, dv) for d = 64. The work is done by the CUDA kernels of ``libfa.so``
 through its C ABI (include/fa.h); this module only allocates outputs and workspace with
 PyTorch and passes pointers and the current stream.
 """
@@ -26,7 +28,10 @@ from ._binding import (  # noqa: F401
     fa_bwd_ex,
     fa_bwd_workspace_size,
     fa_fwd,
+    fa_fwd_block_sparse,
     fa_fwd_ex,
+    fa_fwd_kv,
+    fa_fwd_kv_workspace_size,
     lib,
     strerror,
     version,
@@ -75,6 +80,77 @@ def fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=
                        stream)
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd")
+    return out, lse
+
+
+def fwd_kv(q, k, v, causal: bool = True, scale: float | None = None, n_splits: int = 0,
+           out=None, lse=None, workspace=None):
+    """Queries q [B, H, Tq, d] against keys/values k, v [B, H, Tk, d] through fa_fwd_kv.
+
+    causal aligns bottom-right (query i sees key j iff j ≤ i + Tk − Tq; needs Tq ≤ Tk).
+    n_splits = 0 lets the library choose how many key ranges to spread over CTAs; the
+    workspace for the partial results is allocated here unless one is passed.
+    Returns (o, lse); a row that sees no key has o = 0 and lse = −inf.
+    """
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    if k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q must be [B, H, Tq, d] and k, v [B, H, Tk, d]")
+    B, H, Tq, d = q.shape
+    Tk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, H, Tq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        need = fa_fwd_kv_workspace_size(B, H, Tq, Tk, d, n_splits)
+        if need == 0:
+            raise FAError(FA_ERR_INVALID_ARG, "fa_fwd_kv_workspace_size")
+        if workspace is None and need > 1:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_ptr = None if workspace is None else workspace.data_ptr()
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        rc = fa_fwd_kv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, H, Tq, Tk, d, causal, scale, n_splits, ws_ptr, ws_bytes, stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_kv")
+    return out, lse
+
+
+def fwd_block_sparse(q, k, v, block_mask, causal: bool = False, scale: float | None = None,
+                     out=None, lse=None):
+    """Self-attention with 128×128 blocks switched off by ``block_mask`` (a CUDA uint8
+    tensor [ceil(T/128), ceil(T/128)] shared by all heads, or [B·H, ...] per head;
+    nonzero = compute), through fa_fwd_block_sparse. Returns (o, lse); a row that sees
+    no key has o = 0 and lse = −inf."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    if q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k and v must have the same shape")
+    B, H, T, d = q.shape
+    nb = q_tiles(T)
+    if (not isinstance(block_mask, torch.Tensor) or not block_mask.is_cuda
+            or block_mask.dtype != torch.uint8 or not block_mask.is_contiguous()):
+        raise ValueError("block_mask must be a contiguous CUDA uint8 tensor")
+    if tuple(block_mask.shape[-2:]) != (nb, nb) or block_mask.dim() not in (2, 3):
+        raise ValueError(f"block_mask must be [{nb}, {nb}] or [B*H, {nb}, {nb}]")
+    mask_heads = 1 if block_mask.dim() == 2 else block_mask.shape[0]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        rc = fa_fwd_block_sparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 lse.data_ptr(), block_mask.data_ptr(), mask_heads, B, H, T, d,
+                                 causal, scale, stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_block_sparse")
     return out, lse
 
 

@@ -24,7 +24,8 @@ FA_FLAG_TEST_STARVE_Q = 1
 FA_BWD_NOALLOC_SCRATCH_BYTES = 33554432
 
 # Every symbol include/fa.h declares.
-EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_ex",
+EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_fwd_kv_workspace_size", "fa_fwd_kv",
+           "fa_fwd_block_sparse", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_ex",
            "fa_bwd_noalloc", "fa_strerror", "fa_version")
 
 _lock = threading.Lock()
@@ -53,6 +54,12 @@ def lib() -> ctypes.CDLL:
                                     ctypes.c_ulonglong, ctypes.c_uint, vp]
             L.fa_fwd_ex.restype = i
             sz = ctypes.c_size_t
+            L.fa_fwd_kv_workspace_size.argtypes = [i, i, i, i, i, i]
+            L.fa_fwd_kv_workspace_size.restype = sz
+            L.fa_fwd_kv.argtypes = [vp] * 5 + [i, i, i, i, i, i, f, i, vp, sz, vp]
+            L.fa_fwd_kv.restype = i
+            L.fa_fwd_block_sparse.argtypes = [vp] * 6 + [i, i, i, i, i, i, f, vp]
+            L.fa_fwd_block_sparse.restype = i
             L.fa_bwd_workspace_size.argtypes = [i, i, i, i]
             L.fa_bwd_workspace_size.restype = sz
             L.fa_bwd.argtypes = [vp] * 10 + [sz, i, i, i, i, i, f, vp]
@@ -109,3 +116,19 @@ def fa_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, 
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, T, d, causal, scale, stream) -> int:
     return lib().fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, T, d,
                                 int(bool(causal)), float(scale), stream)
+
+
+def fa_fwd_kv_workspace_size(B, H, Tq, Tk, d, n_splits) -> int:
+    return int(lib().fa_fwd_kv_workspace_size(B, H, Tq, Tk, d, n_splits))
+
+
+def fa_fwd_kv(q, k, v, o, lse, B, H, Tq, Tk, d, causal, scale, n_splits, workspace,
+              workspace_bytes, stream) -> int:
+    return lib().fa_fwd_kv(q, k, v, o, lse, B, H, Tq, Tk, d, int(bool(causal)), float(scale),
+                           int(n_splits), workspace, int(workspace_bytes), stream)
+
+
+def fa_fwd_block_sparse(q, k, v, o, lse, block_mask, mask_heads, B, H, T, d, causal, scale,
+                        stream) -> int:
+    return lib().fa_fwd_block_sparse(q, k, v, o, lse, block_mask, int(mask_heads), B, H, T, d,
+                                     int(bool(causal)), float(scale), stream)

@@ -144,6 +144,7 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
   if (!enc) return FA_ERR_LAUNCH;
 
   fa::FwdLaunch a;
+  a.p = fa::FwdParams{};  // the general-form fields stay zero on this path
   if (!encode_map(enc, &a.tm_q, q, T, d, static_cast<int>(BH)) ||
       !encode_map(enc, &a.tm_k, k, T, d, static_cast<int>(BH)) ||
       !encode_map(enc, &a.tm_v, v, T, d, static_cast<int>(BH)))

@@ -1,0 +1,34 @@
+// Instantiations of the general-form attention forward (and its merge) for head dim 64.
+#include <atomic>
+
+#include "fa_launch.h"
+
+namespace fa {
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_gen(const FwdLaunch& a, unsigned combine_grid) {
+  auto* fn = &fa_fwd_kernel<D, CAUSAL, true>;
+  const int smem = Cfg<D>::kSmemBytes;
+  // The shared-memory opt-in is a per-device attribute: set it once per device.
+  static std::atomic<uint64_t> done[kMaxDevices / 64 + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const uint64_t bit = 1ull << (dev % 64);
+  if (!(done[dev / 64].load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    done[dev / 64].fetch_or(bit, std::memory_order_acq_rel);
+  }
+  fn<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || a.p.n_splits <= 1) return e;
+  fa_fwd_combine_kernel<D><<<combine_grid, 256, 0, a.stream>>>(
+      a.p.o_part, a.p.lse_part, a.p.o, a.p.lse, a.p.n_splits, a.p.BH * a.p.T);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_gen_d64(const FwdLaunch& a, bool causal, unsigned combine_grid) {
+  return causal ? launch_gen<64, true>(a, combine_grid) : launch_gen<64, false>(a, combine_grid);
+}
+
+}  // namespace fa

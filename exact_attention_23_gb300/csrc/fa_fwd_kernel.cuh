@@ -107,6 +107,16 @@ struct FwdParams {
   float scale_log2;   // scale · log2(e)
   uint64_t timeout_ns;
   uint32_t flags;
+  // General form only (GEN kernels; T above is then the query length Tq):
+  int Tk;             // key length
+  int n_qt;           // ceil(Tq/128) query tiles
+  int kv_off;         // Tk − Tq: causal visibility is key ≤ query + kv_off (bottom-right)
+  int n_splits;       // key ranges per query unit (partial results when > 1)
+  int kt_per_split;   // K tiles per range
+  const uint8_t* bmask;  // optional [mask heads][n_qt][n_kv] block mask (nonzero = keep)
+  int bmask_heads;    // 1 (shared) or BH
+  float* o_part;      // n_splits > 1: [n_splits][BH][Tq][D] fp32 normalised partial O
+  float* lse_part;    // n_splits > 1: [n_splits][BH][Tq] fp32 partial LSE (−∞: no key)
 };
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
@@ -117,8 +127,16 @@ __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 // together. CTA c takes the units of round r = 0, 1, 2, ... at position c in even rounds
 // and G−1−c in odd rounds (G = grid size). Over a list sorted by cost this zig-zag gives
 // every CTA nearly the same total work without any shared counter.
+//
+// General form (GEN): a unit is (head, query unit, key range). Its steps walk the K tiles
+// of the range that at least one of its Q tiles uses; tile i uses K tile kt when the tile
+// exists, kt is not past the last key its rows may see (causal, bottom-right), and the
+// block mask keeps (qt, kt). nkv[i] counts those steps for tile i, n_steps the union.
 struct Unit {
   int bh, qt0, nkv[2], n_steps;
+  int kb, ke;     // K-tile range [kb, ke) (dense: [0, n_steps))
+  int last[2];    // last K tile visible to tile i (GEN, causal)
+  int split, mh;  // key-range index; block-mask head
 };
 
 __device__ __forceinline__ int unit_index(int round, int cta, int grid) {
@@ -126,8 +144,45 @@ __device__ __forceinline__ int unit_index(int round, int cta, int grid) {
 }
 
 template <bool CAUSAL>
+__device__ __forceinline__ bool gen_active(const FwdParams& p, const Unit& u, int i, int kt) {
+  const int qt = u.qt0 + i;
+  if (i >= p.tiles_per_cta || qt * kBlockM >= p.T) return false;
+  if (CAUSAL && kt > (i ? u.last[1] : u.last[0])) return false;
+  if (p.bmask != nullptr)
+    return p.bmask[(static_cast<size_t>(u.mh) * p.n_qt + qt) * p.n_kv + kt] != 0;
+  return true;
+}
+
+template <bool CAUSAL, bool GEN>
 __device__ __forceinline__ Unit unit_of(const FwdParams& p, int L) {
   Unit u;
+  if constexpr (GEN) {
+    // bh fastest, then key range, then query unit (no cost order: ranges are balanced)
+    u.bh = L % p.BH;
+    const int rest = L / p.BH;
+    u.split = rest % p.n_splits;
+    u.qt0 = (rest / p.n_splits) * p.tiles_per_cta;
+    u.kb = u.split * p.kt_per_split;
+    u.ke = min(p.n_kv, u.kb + p.kt_per_split);
+    u.mh = (p.bmask_heads == 1) ? 0 : u.bh;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int last_row = min((u.qt0 + i) * kBlockM + kBlockM - 1, p.T - 1);
+      u.last[i] = CAUSAL ? min(p.n_kv - 1, (last_row + p.kv_off) / kBlockN) : p.n_kv - 1;
+      u.nkv[i] = 0;
+    }
+    u.n_steps = 0;
+    for (int kt = u.kb; kt < u.ke; ++kt) {
+      const bool a0 = gen_active<CAUSAL>(p, u, 0, kt), a1 = gen_active<CAUSAL>(p, u, 1, kt);
+      u.nkv[0] += a0;
+      u.nkv[1] += a1;
+      u.n_steps += (a0 || a1);
+    }
+    return u;
+  }
+  u.kb = 0;
+  u.split = 0;
+  u.mh = 0;
   const int per_group = p.n_units * p.head_group;
   const int grp = L / per_group;
   const int within = L - grp * per_group;
@@ -141,10 +196,34 @@ __device__ __forceinline__ Unit unit_of(const FwdParams& p, int L) {
     u.nkv[i] = (i >= p.tiles_per_cta || qt * kBlockM >= p.T) ? 0 : (CAUSAL ? qt + 1 : p.n_kv);
   }
   u.n_steps = max(u.nkv[0], u.nkv[1]);
+  u.ke = u.n_steps;
+  u.last[0] = u.last[1] = 0;
   return u;
 }
 
-template <int D, bool CAUSAL>
+// Step → K tile. Dense: step j is K tile j and tile i is active while j < nkv[i]. GEN: the
+// cursor kt advances to the next K tile that the tile (i ≥ 0) or any tile (i < 0) uses.
+template <bool CAUSAL, bool GEN>
+__device__ __forceinline__ int next_kt(const FwdParams& p, const Unit& u, int kt, int i) {
+  if constexpr (!GEN) {
+    return kt + 1;
+  } else {
+    for (++kt; kt < u.ke; ++kt) {
+      const bool a = (i >= 0) ? gen_active<CAUSAL>(p, u, i, kt)
+                              : (gen_active<CAUSAL>(p, u, 0, kt) || gen_active<CAUSAL>(p, u, 1, kt));
+      if (a) break;
+    }
+    return kt;
+  }
+}
+
+template <bool CAUSAL, bool GEN>
+__device__ __forceinline__ bool tile_active(const FwdParams& p, const Unit& u, int i, int kt, int j) {
+  if constexpr (!GEN) return j < u.nkv[i];
+  else return gen_active<CAUSAL>(p, u, i, kt);
+}
+
+template <int D, bool CAUSAL, bool GEN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -211,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; ok && r * grid < p.total_units; ++r) {
       const int L = unit_index(r, cta, grid);
       if (L >= p.total_units) continue;
-      const Unit u = unit_of<CAUSAL>(p, L);
+      const Unit u = unit_of<CAUSAL, GEN>(p, L);
       const int qb = qn % C::kQBufs;
       if (qn >= C::kQBufs &&
           !mbar_wait_warp(&bars->q_empty[qb], ((qn / C::kQBufs) - 1) & 1, wc)) { ok = false; break; }
@@ -225,7 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       ++qn;
+      int kt = u.kb - 1;
       for (int j = 0; j < u.n_steps; ++j, ++g) {
+        kt = next_kt<CAUSAL, GEN>(p, u, kt, -1);
         const int st = g % C::kStages;
         const int use = g / C::kStages;
         if (use > 0 && !mbar_wait_warp(&bars->kv_empty[st], (use - 1) & 1, wc)) { ok = false; break; }
@@ -235,12 +316,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int s = 0; s < C::kSub; ++s)
             tma_load_3d_hint(smem + C::kKOff + st * C::kTileBytes + s * C::kSubBytes, &tm_k,
-                             &bars->k_full[st], s * 64, j * kBlockN, u.bh, keep);
+                             &bars->k_full[st], s * 64, kt * kBlockN, u.bh, keep);
           mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
 #pragma unroll
           for (int s = 0; s < C::kSub; ++s)
             tma_load_3d_hint(smem + C::kVOff + st * C::kTileBytes + s * C::kSubBytes, &tm_v,
-                             &bars->v_full[st], s * 64, j * kBlockN, u.bh, keep);
+                             &bars->v_full[st], s * 64, kt * kBlockN, u.bh, keep);
         }
         __syncwarp();
       }
@@ -292,16 +373,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; ok && r * grid < p.total_units; ++r) {
         const int L = unit_index(r, cta, grid);
         if (L >= p.total_units) continue;
-        const Unit u = unit_of<CAUSAL>(p, L);
+        const Unit u = unit_of<CAUSAL, GEN>(p, L);
         const int qb = qn % C::kQBufs;
         if (!mbar_wait_warp(&bars->q_full[qb], (qn / C::kQBufs) & 1, wc)) { ok = false; break; }
+        int kt = u.kb - 1;
         for (int j = 0; j < u.n_steps; ++j, ++g) {
+          kt = next_kt<CAUSAL, GEN>(p, u, kt, -1);
           const int st = g % C::kStages;
           if (!mbar_wait_warp(&bars->k_full[st], (g / C::kStages) & 1, wc)) { ok = false; break; }
           tc_fence_after_sync();
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            if (j >= u.nkv[i]) continue;
+            if (!tile_active<CAUSAL, GEN>(p, u, i, kt, j)) continue;
             if (ns[i] > 0) {
               // S_i may be overwritten once its softmax has read it (P in its own columns)
               // or, when P_i lives in S_i's columns, once P_i·V has consumed P_i.
@@ -347,14 +430,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; ok && r * grid < p.total_units; ++r) {
         const int L = unit_index(r, cta, grid);
         if (L >= p.total_units) continue;
-        const Unit u = unit_of<CAUSAL>(p, L);
+        const Unit u = unit_of<CAUSAL, GEN>(p, L);
+        int kt = u.kb - 1;
+        int jt[2] = {0, 0};   // steps of this unit in which tile i was active
         for (int j = 0; j < u.n_steps; ++j, ++g) {
+          kt = next_kt<CAUSAL, GEN>(p, u, kt, -1);
           const int st = g % C::kStages;
           if (!mbar_wait_warp(&bars->v_full[st], (g / C::kStages) & 1, wc)) { ok = false; break; }
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            if (j >= u.nkv[i]) continue;
-            if (j == 0 && nunits[i] > 0) {
+            if (!tile_active<CAUSAL, GEN>(p, u, i, kt, j)) continue;
+            if (jt[i] == 0 && nunits[i] > 0) {
               // This unit's first P·V overwrites O_i: the previous unit's O_i must have
               // been read out.
               if (!mbar_wait_warp(&bars->o_free[i], (nunits[i] - 1) & 1, wc)) { ok = false; break; }
@@ -362,8 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait_warp(&bars->p_full[i], np[i] & 1, wc)) { ok = false; break; }
             FA_TRACE(11 + i, j);
             tc_fence_after_sync();
-            issue_pv(i, st, j > 0);
+            issue_pv(i, st, jt[i] > 0);
             ++np[i];
+            ++jt[i];
             FA_TRACE(14 + i, j);
           }
           if (!ok) break;
@@ -387,42 +474,96 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_o = tmem + lane_off + C::col_o(wg);
     const uint32_t t_p = tmem + lane_off + C::col_p(wg);
     const float c = p.scale_log2;
-    const uint32_t nan2 = 0x7FC07FC0u;  // two bf16 quiet NaNs
 
     int gs = 0;     // S_i consumed (= P_i produced) so far over this CTA's units
     bool ok = true;
     for (int r = 0; r * grid < p.total_units; ++r) {
       const int L = unit_index(r, cta, grid);
       if (L >= p.total_units) continue;
-      const Unit u = unit_of<CAUSAL>(p, L);
-      const int n = u.nkv[wg];
-      if (n == 0) continue;
+      const Unit u = unit_of<CAUSAL, GEN>(p, L);
+      // (ternaries, not u.nkv[wg]: a runtime index would move the unit to local memory)
+      const int n = wg ? u.nkv[1] : u.nkv[0];
       const int qt = u.qt0 + wg;
       const int q_row = qt * kBlockM + row;
+      const bool tile_exists = wg < p.tiles_per_cta && qt * kBlockM < p.T;
+      if (n == 0 && !(GEN && tile_exists)) continue;
       const size_t row_idx = static_cast<size_t>(u.bh) * static_cast<size_t>(p.T) +
                              static_cast<size_t>(q_row);
       const bool in_range = q_row < p.T;
       uint4* orow = reinterpret_cast<uint4*>(p.o + row_idx * D);
+      // General form with several key ranges: this unit's fp32 partial row.
+      const bool partial = GEN && p.n_splits > 1;
+      const size_t part_idx =
+          (static_cast<size_t>(u.split) * p.BH + u.bh) * static_cast<size_t>(p.T) + q_row;
+      // Writes an output row: fp32 values scaled by mul (partial) or bf16 (final).
+      auto write_row = [&](const uint32_t* r, int c0, float mul) {
+        if (!in_range) return;
+        if (partial) {
+          float4* prow = reinterpret_cast<float4*>(p.o_part + part_idx * D + c0);
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            prow[t] = make_float4(u2f(r[4 * t]) * mul, u2f(r[4 * t + 1]) * mul,
+                                  u2f(r[4 * t + 2]) * mul, u2f(r[4 * t + 3]) * mul);
+        } else {
+          uint32_t ob[16];
+#pragma unroll
+          for (int t = 0; t < 16; ++t)
+            ob[t] = pack_bf16x2(u2f(r[2 * t]) * mul, u2f(r[2 * t + 1]) * mul);
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            orow[c0 / 8 + t] = make_uint4(ob[4 * t], ob[4 * t + 1], ob[4 * t + 2], ob[4 * t + 3]);
+        }
+      };
+      auto write_lse = [&](float v) {
+        if (!in_range) return;
+        if (partial) p.lse_part[part_idx] = v;
+        else p.lse[row_idx] = v;
+      };
+      // A row that saw no key (general form: O = 0, LSE = −∞) or a failed unit (NaN).
+      auto write_const_row = [&](uint32_t bits) {
+        if (!in_range) return;
+        if (partial) {
+          float4* prow = reinterpret_cast<float4*>(p.o_part + part_idx * D);
+          const float f = u2f(bits);
+#pragma unroll
+          for (int t = 0; t < D / 4; ++t) prow[t] = make_float4(f, f, f, f);
+        } else {
+          const uint32_t b2 = pack_bf16x2(u2f(bits), u2f(bits));
+#pragma unroll
+          for (int t = 0; t < D / 8; ++t) orow[t] = make_uint4(b2, b2, b2, b2);
+        }
+      };
       if (!ok) {
         // A wait gave up earlier: mark every row this warpgroup owns as failed.
-        if (in_range) {
-#pragma unroll
-          for (int t = 0; t < D / 8; ++t) orow[t] = make_uint4(nan2, nan2, nan2, nan2);
-          p.lse[row_idx] = __uint_as_float(0x7FC00000u);
-        }
+        write_const_row(0x7FC00000u);
+        write_lse(__uint_as_float(0x7FC00000u));
+        continue;
+      }
+      if (n == 0) {  // general form: this tile uses no K tile of the range
+        write_const_row(0u);
+        write_lse(-INFINITY);
         continue;
       }
 
       float m_ref = -INFINITY;  // reference max (base-2 scaled units) shared by O and l
       float l = 0.0f;
+      int kt = u.kb - 1;
       for (int j = 0; j < n; ++j, ++gs) {
+        kt = next_kt<CAUSAL, GEN>(p, u, kt, wg);
         if (!mbar_wait_warp(&bars->s_full[wg], gs & 1, wc)) { ok = false; break; }
         FA_TRACE(30 + wg, j);
         tc_fence_after_sync();
-        const int k0 = j * kBlockN;
-        const bool masked = (CAUSAL && j == qt) || (k0 + kBlockN > p.T);
-        // Keys past the end of the sequence, and (diagonal tile) keys after this query.
-        const int lim = (CAUSAL ? min(q_row + 1, p.T) : p.T) - k0;
+        const int k0 = kt * kBlockN;
+        // Keys past the end of the sequence, and (causal) keys after this query.
+        int lim;
+        bool masked;
+        if constexpr (GEN) {
+          lim = (CAUSAL ? min(q_row + 1 + p.kv_off, p.Tk) : p.Tk) - k0;
+          masked = lim < kBlockN;
+        } else {
+          lim = (CAUSAL ? min(q_row + 1, p.T) : p.T) - k0;
+          masked = (CAUSAL && kt == qt) || (k0 + kBlockN > p.T);
+        }
 
         // S in two halves: the second half loads while the first is masked and maxed.
         uint32_t s[kBlockN];
@@ -481,7 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // p = 2^(s·c − m_ref) on fp32 pairs; row sum in fp32; P kept as bf16 pairs.
         const uint64_t c2 = f2_pack(c, c);
-        const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
+        // (general form: a row with no visible key so far keeps m_ref = −∞; its p are 0)
+        const float m_use = (GEN && m_ref == -INFINITY) ? 0.0f : m_ref;
+        const uint64_t nm2 = f2_pack(-m_use, -m_use);
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
         uint32_t pk[kBlockN / 2];
 #pragma unroll
@@ -537,36 +680,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       FA_TRACE(24 + wg, 0);
       if (good) {
         tc_fence_after_sync();
-        const float inv_l = 1.0f / l;
+        const bool empty = GEN && !(l > 0.0f);  // general form: the row saw no key
+        const float inv_l = empty ? 0.0f : 1.0f / l;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t r[32];
           tmem_ld32(t_o + c0, r);
           tmem_ld_wait();
           reg_fence32(r);
-          if (in_range) {
-            uint32_t ob[16];
-#pragma unroll
-            for (int t = 0; t < 16; ++t)
-              ob[t] = pack_bf16x2(u2f(r[2 * t]) * inv_l, u2f(r[2 * t + 1]) * inv_l);
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-              orow[c0 / 8 + t] = make_uint4(ob[4 * t], ob[4 * t + 1], ob[4 * t + 2], ob[4 * t + 3]);
-          }
+          write_row(r, c0, inv_l);
         }
         // O_i has been read: the next unit's first P·V may overwrite it.
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->o_free[wg]);
-        if (in_range) p.lse[row_idx] = (m_ref + log2f(l)) * 0.69314718055994530942f;
+        write_lse(empty ? -INFINITY : (m_ref + log2f(l)) * 0.69314718055994530942f);
         FA_TRACE(26 + wg, 0);
       } else {
         ok = false;
-        if (in_range) {
-#pragma unroll
-          for (int t = 0; t < D / 8; ++t) orow[t] = make_uint4(nan2, nan2, nan2, nan2);
-          p.lse[row_idx] = __uint_as_float(0x7FC00000u);
-        }
+        write_const_row(0x7FC00000u);
+        write_lse(__uint_as_float(0x7FC00000u));
       }
     }
   }
@@ -577,6 +710,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// Merge of the key-range partial results of the general form: with M = max_s LSE_s and
+// w_s = exp(LSE_s − M), O = Σ w_s·O_s / Σ w_s (bf16) and LSE = M + ln Σ w_s; a row that no
+// range saw gets O = 0 and LSE = −∞. This is the merge of results over disjoint key blocks
+// that the first FlashAttention's outer K/V loop needed ("手写 FlashAttention", step ③),
+// used here to spread one query tile's keys over several CTAs. One thread per (row, 8
+// columns); rows = B·H·Tq.
+template <int D>
+__global__ void __launch_bounds__(256) fa_fwd_combine_kernel(const float* __restrict__ o_part,
+                                                             const float* __restrict__ lse_part,
+                                                             __nv_bfloat16* __restrict__ o,
+                                                             float* __restrict__ lse,
+                                                             int n_splits, int rows) {
+  constexpr int L = D / 8;
+  const size_t total = static_cast<size_t>(rows) * L;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += stride) {
+    const size_t row = idx / L;
+    const int c8 = static_cast<int>(idx % L);
+    float m = -INFINITY;
+    for (int s = 0; s < n_splits; ++s) m = fmaxf(m, lse_part[static_cast<size_t>(s) * rows + row]);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float wsum = 0.f;
+    if (m != -INFINITY) {
+      for (int s = 0; s < n_splits; ++s) {
+        const float ls = lse_part[static_cast<size_t>(s) * rows + row];
+        if (ls == -INFINITY) continue;
+        const float w = expf(ls - m);
+        wsum += w;
+        const float4* src = reinterpret_cast<const float4*>(
+            o_part + (static_cast<size_t>(s) * rows + row) * D + c8 * 8);
+        const float4 a = src[0], b = src[1];
+        acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+        acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    uint4 out;
+    out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    out.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    out.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4*>(o + row * D + c8 * 8) = out;
+    if (c8 == 0) lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
   }
 }
 

@@ -23,6 +23,11 @@ struct FwdLaunch {
 cudaError_t launch_fwd_d64(const FwdLaunch& a, bool causal);
 cudaError_t launch_fwd_d128(const FwdLaunch& a, bool causal);
 
+// General form (Tq ≠ Tk, bottom-right causal, block masks, key ranges): the forward kernel
+// with GEN = true, then, when a.p.n_splits > 1, the merge of the partial results.
+cudaError_t launch_fwd_gen_d64(const FwdLaunch& a, bool causal, unsigned combine_grid);
+cudaError_t launch_fwd_gen_d128(const FwdLaunch& a, bool causal, unsigned combine_grid);
+
 struct BwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
   BwdParams p;

@@ -90,6 +90,59 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
 
 /*
  * ---------------------------------------------------------------------------------------
+ * General forms of the forward.
+ *
+ * Both compute, for every b, h, the attention of Tq query rows over Tk key rows with a
+ * visibility mask, in the same tiled online-softmax way as fa_fwd:
+ *
+ *   query i sees key j  iff  (causal == 0 or j ≤ i + Tk − Tq)        [bottom-right causal]
+ *                        and (no block mask or mask[i/128][j/128] ≠ 0)
+ *
+ * A row that sees no key at all gets O = 0 and LSE = −∞. Layouts, alignment, ownership,
+ * asynchrony and error behaviour are those of fa_fwd (q, o: [B, H, Tq, d]; k, v:
+ * [B, H, Tk, d]; lse: [B, H, Tq]); d ∈ {64, 128}.
+ * ---------------------------------------------------------------------------------------
+ */
+
+/*
+ * fa_fwd_kv — Tq queries against Tk keys, e.g. new tokens (or one decoded token,
+ * Tq = 1) against the K/V of every earlier token, which generation keeps ("手写
+ * FlashAttention" step ①). causal requires Tq ≤ Tk. When B·H·ceil(Tq/128) query tiles
+ * leave SMs idle, the key range is split into n_splits ranges processed by different
+ * CTAs; each writes a partial result (normalised O, LSE) to the workspace and a second
+ * kernel merges them with weights exp(LSE_s − max LSE) — the merge over K/V blocks that
+ * step ③ of the same page attributes to the first FlashAttention's outer loop.
+ *
+ *   n_splits  : key ranges; 0 picks a number from the SM count of the current device
+ *   workspace : device memory, 256-byte aligned, at least fa_fwd_kv_workspace_size(...)
+ *               bytes, owned by the caller; unused (may be NULL) when one range is used.
+ *               Must not overlap any argument or be used by a concurrent call.
+ */
+size_t fa_fwd_kv_workspace_size(int B, int H, int Tq, int Tk, int d, int n_splits);
+int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int Tq, int Tk, int d, int causal, float scale, int n_splits, void* workspace,
+              size_t workspace_bytes, void* stream);
+/* fa_fwd_kv_workspace_size returns the bytes needed for these sizes and n_splits (0: the
+ * automatic choice on the current device), 1 when no workspace is needed, and 0 for
+ * unsupported sizes or (automatic choice) no usable device. */
+
+/*
+ * fa_fwd_block_sparse — self-attention (Tq = Tk = T) in which whole 128×128 blocks of the
+ * score matrix are switched off by a block mask and never computed: the generalisation of
+ * skipping fully masked causal blocks ("内核案例研究：Flash Attention", "块稀疏注意力 V2 和
+ * V3": a block whose mask is all zero is skipped).
+ *
+ *   block_mask : DEVICE uint8 array [mask_heads][ceil(T/128)][ceil(T/128)], row-major,
+ *                nonzero = compute the block; owned by the caller, not modified
+ *   mask_heads : 1 (one mask for every head) or B·H (one per (b, h), in b-major order)
+ *   causal     : combined with the block mask (element-wise within kept blocks)
+ */
+int fa_fwd_block_sparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const unsigned char* block_mask, int mask_heads, int B, int H, int T,
+                        int d, int causal, float scale, void* stream);
+
+/*
+ * ---------------------------------------------------------------------------------------
  * Backward pass.
  *
  * The gradients of the forward above for an upstream gradient dO = ∂L/∂O:

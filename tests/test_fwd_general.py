@@ -1,0 +1,137 @@
+"""GPU parity of the general forward forms against the fp64 oracle's general form:
+fa_fwd_kv (Tq queries over Tk keys, bottom-right causal, key range split over CTAs with
+the partial results merged) and fa_fwd_block_sparse (128×128 blocks switched off).
+
+Tolerances as for the forward: O max-abs ≤ 2e-2, mean-abs ≤ 1e-3 (+ 2⁻⁹·mean|O_ref| for
+shapes whose rows see few keys, as in test_parity.py), LSE ≤ 1e-3 absolute on rows that see
+a key. Rows that see no key must be exactly O = 0 and LSE = −∞. Inputs: q, k, v drawn by
+inputs.make_qkv at the key length; the queries are the last Tq rows of that q draw (new
+tokens at the end of the sequence)."""
+
+import numpy as np
+import pytest
+
+import oracle
+from exact_attention_23_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_MEAN, LSE_MAX = 2e-2, 1e-3, 1e-3
+
+
+def _compare(o, lse, o_ref, lse_ref, what):
+    live = np.isfinite(lse_ref)
+    assert np.all(np.isfinite(o)), what
+    assert np.array_equal(np.isneginf(lse), ~live), f"{what}: empty rows differ"
+    assert np.all(o[~live] == 0.0), f"{what}: empty rows must be 0"
+    err = np.abs(o - o_ref)
+    mean_bound = O_MEAN + 2.0 ** -9 * float(np.abs(o_ref).mean())
+    assert err.max() <= O_MAX, f"{what}: O max-abs {err.max():.3e}"
+    assert err.mean() <= mean_bound, f"{what}: O mean-abs {err.mean():.3e} > {mean_bound:.3e}"
+    if live.any():
+        lerr = np.abs(lse[live] - lse_ref[live])
+        assert lerr.max() <= LSE_MAX, f"{what}: LSE max-abs {lerr.max():.3e}"
+
+
+def _qkv_kv(B, H, Tq, Tk, d, seed):
+    q, k, v = inputs.make_qkv(B, H, Tk, d, seed)
+    return q[:, :, Tk - Tq:].contiguous() if Tq <= Tk else inputs.make_qkv(B, H, Tq, d, seed)[0], k, v
+
+
+@pytest.mark.parametrize("B,H,Tq,Tk,d,causal,n_splits", [
+    (2, 12, 1, 4096, 64, True, 0),     # decode, automatic ranges
+    (2, 12, 1, 4096, 64, True, 1),     # decode, one range
+    (2, 12, 1, 4096, 64, True, 5),     # uneven ranges
+    (1, 8, 1, 1000, 128, False, 0),
+    (2, 4, 7, 2000, 64, True, 3),
+    (1, 4, 128, 1024, 64, True, 0),
+    (1, 4, 200, 1500, 128, True, 0),   # two query tiles, ragged
+    (1, 2, 300, 300, 64, True, 0),     # Tq = Tk: plain causal attention
+    (1, 2, 1000, 300, 64, False, 2),   # more queries than keys (non-causal)
+])
+def test_fwd_kv_parity(B, H, Tq, Tk, d, causal, n_splits):
+    import torch
+    import exact_attention_23_gb300 as fa
+    q, k, v = _qkv_kv(B, H, Tq, Tk, d, 500 + Tq + Tk + d)
+    o, lse = fa.fwd_kv(q.cuda(), k.cuda(), v.cuda(), causal=causal, n_splits=n_splits)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attention_general(*(inputs.to_f64_numpy(t) for t in (q, k, v)),
+                                              causal, d ** -0.5)
+    _compare(o.float().cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, lse_ref,
+             f"kv B{B} H{H} Tq{Tq} Tk{Tk} d{d} causal={causal} splits={n_splits}")
+
+
+def test_fwd_kv_equal_lengths_matches_fwd():
+    """With Tq = Tk, no split and no mask the general form computes plain attention."""
+    import torch
+    import exact_attention_23_gb300 as fa
+    q, k, v = (t.cuda() for t in inputs.make_qkv(2, 6, 777, 64, 61))
+    for causal in (True, False):
+        o1, l1 = fa.fwd(q, k, v, causal=causal)
+        o2, l2 = fa.fwd_kv(q, k, v, causal=causal, n_splits=1)
+        torch.cuda.synchronize()
+        assert (o1.float() - o2.float()).abs().max().item() <= 2e-2
+        assert (l1 - l2).abs().max().item() <= 1e-3
+
+
+def _mask(nb, heads, density, seed, empty_row=None):
+    r = np.random.default_rng(seed)
+    m = (r.random((heads, nb, nb)) < density).astype(np.uint8)
+    if empty_row is not None:
+        m[:, empty_row, :] = 0
+    return m
+
+
+@pytest.mark.parametrize("T,d,causal,per_head", [
+    (256, 64, False, False),
+    (1000, 64, True, False),
+    (1000, 128, False, True),
+    (2048, 64, True, True),
+    (777, 128, True, False),
+])
+def test_fwd_block_sparse_parity(T, d, causal, per_head):
+    import torch
+    import exact_attention_23_gb300 as fa
+    B, H = 2, 3
+    nb = fa.q_tiles(T)
+    q, k, v = inputs.make_qkv(B, H, T, d, 700 + T + d)
+    heads = B * H if per_head else 1
+    m = _mask(nb, heads, 0.5, T + d, empty_row=1 if nb > 1 else None)
+    mt = torch.from_numpy(m if per_head else m[0]).cuda().contiguous()
+    o, lse = fa.fwd_block_sparse(q.cuda(), k.cuda(), v.cuda(), mt, causal=causal)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attention_general(*(inputs.to_f64_numpy(t) for t in (q, k, v)),
+                                              causal, d ** -0.5, m if per_head else m[0])
+    _compare(o.float().cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, lse_ref,
+             f"block-sparse T{T} d{d} causal={causal} per_head={per_head}")
+
+
+def test_fwd_block_sparse_full_and_causal_masks():
+    """An all-ones mask is plain attention; keeping the blocks on and below the diagonal
+    under causal is plain causal attention (the skipped blocks were fully masked)."""
+    import torch
+    import exact_attention_23_gb300 as fa
+    q, k, v = (t.cuda() for t in inputs.make_qkv(1, 4, 1000, 64, 71))
+    nb = fa.q_tiles(1000)
+    ones = torch.ones((nb, nb), dtype=torch.uint8, device="cuda")
+    tril = torch.tril(ones).contiguous()
+    o_ref, l_ref = fa.fwd(q, k, v, causal=False)
+    o, l = fa.fwd_block_sparse(q, k, v, ones, causal=False)
+    oc_ref, lc_ref = fa.fwd(q, k, v, causal=True)
+    oc, lc = fa.fwd_block_sparse(q, k, v, tril, causal=True)
+    torch.cuda.synchronize()
+    assert (o.float() - o_ref.float()).abs().max().item() <= 2e-2
+    assert (l - l_ref).abs().max().item() <= 1e-3
+    assert (oc.float() - oc_ref.float()).abs().max().item() <= 2e-2
+    assert (lc - lc_ref).abs().max().item() <= 1e-3
+
+
+def test_fwd_block_sparse_all_off():
+    """A mask with every block off: every row is empty (O = 0, LSE = −∞)."""
+    import torch
+    import exact_attention_23_gb300 as fa
+    q, k, v = (t.cuda() for t in inputs.make_qkv(1, 2, 300, 64, 72))
+    zeros = torch.zeros((3, 3), dtype=torch.uint8, device="cuda")
+    o, lse = fa.fwd_block_sparse(q, k, v, zeros, causal=True)
+    torch.cuda.synchronize()
+    assert bool((o == 0).all()) and bool(torch.isneginf(lse).all())

@@ -195,3 +195,63 @@ def test_library_exports_only_the_c_abi(lib):
     funcs = sorted(line.split()[-1] for line in out.splitlines()
                    if len(line.split()) == 3 and line.split()[1] == "T")
     assert funcs == _header_functions()
+
+
+# ---------------------------------------------------------------- general forward forms
+
+def _kv_call(q=A, k=A + SZ, v=A + 2 * SZ, o=A + 3 * SZ, lse=A + 4 * SZ, B=1, H=2, Tq=1, Tk=1000,
+             d=64, causal=1, scale=0.125, n_splits=1, ws=None, ws_bytes=0):
+    return fa.fa_fwd_kv(q, k, v, o, lse, B, H, Tq, Tk, d, causal, scale, n_splits, ws, ws_bytes,
+                        None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Tq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Tk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_INVALID_ARG),
+    (dict(Tq=2000, Tk=1000), fa.FA_ERR_INVALID_ARG),      # causal needs Tq <= Tk
+    (dict(n_splits=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(o=A + 3 * SZ + 2), fa.FA_ERR_MISALIGNED),
+    (dict(o=A + SZ), fa.FA_ERR_INVALID_ARG),              # o aliases k
+])
+def test_fwd_kv_host_validation(lib, kw, want):
+    assert _kv_call(**kw) == want
+
+
+def test_fwd_kv_workspace_size(lib):
+    # explicit splits: S·B·H·Tq·d·4 bytes of partial O plus S·B·H·Tq·4 of LSE, 256-aligned
+    assert fa.fa_fwd_kv_workspace_size(2, 12, 1, 4096, 64, 4) == (
+        -(-4 * 24 * 64 * 4 // 256) * 256 + -(-4 * 24 * 4 // 256) * 256)
+    assert fa.fa_fwd_kv_workspace_size(2, 12, 1, 4096, 64, 1) == 1   # no workspace needed
+    assert fa.fa_fwd_kv_workspace_size(1, 1, 1, 100, 64, 8) == 1     # one K tile: one range
+    assert fa.fa_fwd_kv_workspace_size(1, 1, 0, 100, 64, 2) == 0
+    assert fa.fa_fwd_kv_workspace_size(1, 1, 1, 100, 32, 2) == 0
+
+
+def _bs_call(q=A, k=A + SZ, v=A + 2 * SZ, o=A + 3 * SZ, lse=A + 4 * SZ, mask=A + 5 * SZ,
+             mask_heads=1, B=1, H=2, T=1000, d=64, causal=0, scale=0.125):
+    return fa.fa_fwd_block_sparse(q, k, v, o, lse, mask, mask_heads, B, H, T, d, causal, scale,
+                                  None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(mask=0), fa.FA_ERR_INVALID_ARG),
+    (dict(mask_heads=0), fa.FA_ERR_INVALID_ARG),
+    (dict(mask_heads=3), fa.FA_ERR_INVALID_ARG),           # neither 1 nor B·H
+    (dict(T=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=256), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=A + 4 * SZ + 4), fa.FA_ERR_MISALIGNED),
+])
+def test_fwd_block_sparse_host_validation(lib, kw, want):
+    assert _bs_call(**kw) == want
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="only meaningful on a machine without a CUDA device")
+def test_general_forms_without_device_report_unsupported(lib):
+    assert _kv_call() == fa.FA_ERR_UNSUPPORTED_DEVICE
+    assert _bs_call() == fa.FA_ERR_UNSUPPORTED_DEVICE
+    assert _bs_call(mask_heads=2) == fa.FA_ERR_UNSUPPORTED_DEVICE
+    assert fa.fa_fwd_kv_workspace_size(1, 1, 1, 1000, 64, 0) == 0   # automatic choice needs a device
