@@ -11,7 +11,9 @@ inputs in pinned host memory and the host<->device copies inside the timed regio
 L2: each step touches ~0.8 GB of distinct inputs and outputs (more than 6× the 129 MB L2),
 so every launch reads inputs last touched a full step earlier.
 
-The same line carries a `backward` object: the gradient pass (dQ, dK, dV through fa_bwd)
+The same line carries `decode` (one query per head against a 16k-token KV cache, GB/s),
+`block_sparse` (T = 8192 with half the 128×128 blocks kept, TFLOP/s on kept blocks) and a
+`backward` object: the gradient pass (dQ, dK, dV through fa_bwd)
 timed the same way over the same sweep, K steps, with an upstream gradient dO drawn per T;
 FLOPs are 2.5× the forward's (five T×T×d products instead of two).
 
@@ -290,6 +292,94 @@ def run_reference(args):
 
 # --------------------------------------------------------------------------- GPU arm
 
+DECODE_TK = 16384
+SPARSE_T = 8192
+SPARSE_DENSITY = 0.5
+
+
+def _time_calls(fn, steps, warmup, stream, torch, ws):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    _barrier(ws)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    return _max_over_ranks(a.elapsed_time(b), ws) / steps
+
+
+def _general_forms(args, fa, inputs, torch, dev, stream, bf16_sus, hbm_peak, ws):
+    """Decode (one new query per head against a 16k-token KV cache, B4 H12 d64, key range
+    split over CTAs) and block-sparse self-attention (T = 8192, half of the 128×128 blocks
+    kept at random, non-causal). Inputs are allocated before timing; K steps each."""
+    scale = D ** -0.5
+    out = {}
+    # decode: HBM-bound (reads K and V once): algorithmic bytes = K, V, q in, o and lse out
+    q, k, v = (t.to(dev) for t in inputs.make_qkv(B, H, DECODE_TK, D, seed=20))
+    qd = q[:, :, -1:].contiguous()
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, 1), dtype=torch.float32, device=dev)
+    need = fa.fa_fwd_kv_workspace_size(B, H, 1, DECODE_TK, D, 0)
+    wsb = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+
+    def dec():
+        rc = fa.fa_fwd_kv(qd.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          B, H, 1, DECODE_TK, D, 1, scale, 0, wsb.data_ptr(), wsb.numel(),
+                          stream.cuda_stream)
+        if rc != fa.FA_OK:
+            raise fa.FAError(rc, "fa_fwd_kv")
+    # L2: K and V are 201 MB (> L2), so each call reads them from HBM
+    ms = _time_calls(dec, args.steps, args.warmup, stream, torch, ws)
+    byts = 2.0 * B * H * DECODE_TK * D * 2 + B * H * D * 2 * 2 + B * H * 4
+    gbs = ws * byts / ms / 1e6
+    out["decode"] = {
+        "metric": "decode GB/s (bf16, B4 H12 d64, 1 query vs 16384 cached keys, causal)",
+        "value": gbs, "unit": "GB/s", "us_per_call": ms * 1e3, "steps": args.steps,
+        "roofline": {"bound": "hbm", "achieved": gbs / ws, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": gbs / ws / hbm_peak, "traffic": None,
+                     "algorithmic_bytes": byts,
+                     "kernel": "fa_fwd_kernel<64,causal,general> over split key ranges + "
+                               "fa_fwd_combine_kernel; achieved over the whole fa_fwd_kv call"},
+        "gpu_launches": 2 * args.steps,
+    }
+    del q, k, v, qd, o, lse, wsb
+    # block-sparse: tensor-bound on the kept blocks
+    q, k, v = (t.to(dev) for t in inputs.make_qkv(B, H, SPARSE_T, D, seed=21))
+    nb = fa.q_tiles(SPARSE_T)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(22)
+    mask = (torch.rand((nb, nb), generator=g) < SPARSE_DENSITY).to(torch.uint8).to(dev)
+    kept = int(mask.sum().item())
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, SPARSE_T), dtype=torch.float32, device=dev)
+
+    def sparse():
+        rc = fa.fa_fwd_block_sparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr(), mask.data_ptr(), 1, B, H, SPARSE_T, D, 0,
+                                    scale, stream.cuda_stream)
+        if rc != fa.FA_OK:
+            raise fa.FAError(rc, "fa_fwd_block_sparse")
+    ms = _time_calls(sparse, args.steps, args.warmup, stream, torch, ws)
+    flops = 4.0 * B * H * 128 * 128 * D * kept
+    tf = ws * flops / ms / 1e9
+    out["block_sparse"] = {
+        "metric": "block-sparse attn fwd TFLOP/s on kept blocks (bf16, B4 H12 d64, T 8192, "
+                  "50% random 128x128 blocks, non-causal)",
+        "value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "kept_blocks": kept,
+        "blocks": nb * nb, "steps": args.steps,
+        "roofline": {"bound": "tensor", "achieved": tf / ws, "peak": bf16_sus, "unit": "TFLOP/s",
+                     "frac": tf / ws / bf16_sus, "traffic": None,
+                     "kernel": "fa_fwd_kernel<64,non-causal,general> with a block mask; FLOPs "
+                               "= 4·B·H·128²·d per kept block"},
+        "gpu_launches": args.steps,
+    }
+    return out
+
 def run_gpu(args):
     import torch
 
@@ -412,8 +502,10 @@ def run_gpu(args):
         bper_T.append({"T": T, "ms": ms, "tflops": fl / ms / 1e9,
                        "frac_of_sustained": fl / ms / 1e9 / bf16_sus})
     bdom = max(bper_T, key=lambda r: r["T"])
-    launches += 3 * args.steps * len(bsets)
     del bsets
+
+    # ---- general forms: decode against a KV cache (split key ranges), block-sparse
+    extra = _general_forms(args, fa, inputs, torch, dev, stream, bf16_sus, hbm_peak, ws)
 
     # ---- end to end: pinned host inputs -> device -> forward -> host, per step
     e2e_steps = max(1, min(args.steps, 10))
@@ -482,6 +574,7 @@ def run_gpu(args):
             "gpu_launches": launches,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            **extra,
             "backward": {
                 "metric": BWD_METRIC, "value": bvalue, "unit": "TFLOP/s",
                 "ms_per_step": b_ms / args.steps, "steps": args.steps,
