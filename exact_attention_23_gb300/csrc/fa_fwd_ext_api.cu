@@ -29,6 +29,30 @@ int auto_splits(long long BH, long long n_qt, long long n_kt, int sms) {
   return static_cast<int>(std::max<long long>(1, std::min<long long>(s, 64)));
 }
 
+// Decode (one query row per head): as many key ranges as fit one wave of resident CTAs
+// (a second, partial wave would double the time), each range at least 256 keys.
+int decode_splits(long long BH, long long Tk, int sms) {
+  long long s = static_cast<long long>(sms) * fa::kDecCtasPerSm / BH;
+  s = std::min<long long>(s, std::max<long long>(1, Tk / 256));
+  return static_cast<int>(std::max<long long>(1, std::min<long long>(s, 1024)));
+}
+
+// Key ranges actually used for these sizes (requested > 0, or the automatic choice), with
+// no empty range.
+int effective_splits(long long BH, long long Tq, long long Tk, int requested, int sms) {
+  const long long n_qt = (Tq + 127) / 128, n_kt = (Tk + 127) / 128;
+  if (Tq == 1) {
+    long long s = requested ? requested : decode_splits(BH, Tk, sms);
+    s = std::min<long long>(s, Tk);
+    const long long per = (Tk + s - 1) / s;
+    return static_cast<int>((Tk + per - 1) / per);
+  }
+  long long s = requested ? requested : auto_splits(BH, n_qt, n_kt, sms);
+  s = std::min<long long>(s, n_kt);
+  const long long per = (n_kt + s - 1) / s;
+  return static_cast<int>((n_kt + per - 1) / per);
+}
+
 size_t partial_bytes(long long BH, long long Tq, int d, int splits) {
   if (splits <= 1) return 0;
   return round_up256(static_cast<size_t>(splits) * BH * Tq * d * 4) +
@@ -140,13 +164,14 @@ size_t fa_fwd_kv_workspace_size(int B, int H, int Tq, int Tk, int d, int n_split
   const long long BH = static_cast<long long>(B) * H;
   const long long n_qt = (static_cast<long long>(Tq) + 127) / 128;
   const long long n_kt = (static_cast<long long>(Tk) + 127) / 128;
-  int splits = n_splits;
-  if (splits == 0) {
-    int dev = -1, sms = 0;
+  (void)n_qt;
+  (void)n_kt;
+  int sms = 0;
+  if (n_splits == 0) {
+    int dev = -1;
     if (check_device(&dev, &sms) != FA_OK) return 0;
-    splits = auto_splits(BH, n_qt, n_kt, sms);
   }
-  splits = static_cast<int>(std::min<long long>(splits, n_kt));
+  const int splits = effective_splits(BH, Tq, Tk, n_splits, sms);
   const size_t bytes = partial_bytes(BH, Tq, d, splits);
   return bytes == 0 ? 1 : bytes;  // nonzero: "supported, needs (almost) nothing"
 }
@@ -162,10 +187,7 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
   st = check_device(&dev, &sms);
   if (st != FA_OK) return st;
   const long long BH = static_cast<long long>(B) * H;
-  const long long n_qt = (static_cast<long long>(Tq) + 127) / 128;
-  const long long n_kt = (static_cast<long long>(Tk) + 127) / 128;
-  int splits = n_splits ? n_splits : auto_splits(BH, n_qt, n_kt, sms);
-  splits = static_cast<int>(std::min<long long>(splits, n_kt));
+  const int splits = effective_splits(BH, Tq, Tk, n_splits, sms);
   const size_t need = partial_bytes(BH, Tq, d, splits);
   if (need > 0) {
     if (!workspace || workspace_bytes < need) return FA_ERR_INVALID_ARG;
@@ -175,6 +197,31 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
         overlaps(workspace, need, v, kb) || overlaps(workspace, need, o, qb) ||
         overlaps(workspace, need, lse, static_cast<size_t>(BH) * Tq * 4))
       return FA_ERR_INVALID_ARG;
+  }
+  if (Tq == 1) {
+    // One query row per head: a streaming kernel on the CUDA cores (the query sees every
+    // key under bottom-right causal alignment, so causal changes nothing here).
+    fa::DecodeParams dp{};
+    dp.q = static_cast<const __nv_bfloat16*>(q);
+    dp.k = static_cast<const __nv_bfloat16*>(k);
+    dp.v = static_cast<const __nv_bfloat16*>(v);
+    dp.o = static_cast<__nv_bfloat16*>(o);
+    dp.lse = lse;
+    dp.BH = static_cast<int>(BH);
+    dp.Tk = Tk;
+    dp.n_splits = splits;
+    dp.keys_per_split = static_cast<int>((static_cast<long long>(Tk) + splits - 1) / splits);
+    dp.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    if (splits > 1) {
+      uint8_t* ws = static_cast<uint8_t*>(workspace);
+      dp.o_part = reinterpret_cast<float*>(ws);
+      dp.lse_part = reinterpret_cast<float*>(
+          ws + round_up256(static_cast<size_t>(splits) * BH * d * 4));
+    }
+    if (BH * splits > INT32_MAX) return FA_ERR_INVALID_ARG;
+    const cudaError_t e = fa::launch_decode(dp, d, static_cast<unsigned>(sms) * 8u,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
   }
   GenArgs g{q, k, v, o, lse, nullptr, 1, B, H, Tq, Tk, d, causal, scale, splits, workspace,
             workspace_bytes, stream, nullptr, 0ull};

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "fa_bwd_kernel.cuh"
+#include "fa_decode_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -27,6 +28,10 @@ cudaError_t launch_fwd_d128(const FwdLaunch& a, bool causal);
 // with GEN = true, then, when a.p.n_splits > 1, the merge of the partial results.
 cudaError_t launch_fwd_gen_d64(const FwdLaunch& a, bool causal, unsigned combine_grid);
 cudaError_t launch_fwd_gen_d128(const FwdLaunch& a, bool causal, unsigned combine_grid);
+
+// Decode (Tq = 1) on the CUDA cores: grid B·H × n_splits, then the merge when split.
+cudaError_t launch_decode(const DecodeParams& p, int d, unsigned combine_grid,
+                          cudaStream_t stream);
 
 struct BwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;

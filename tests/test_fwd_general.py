@@ -1,6 +1,7 @@
 """GPU parity of the general forward forms against the fp64 oracle's general form:
 fa_fwd_kv (Tq queries over Tk keys, bottom-right causal, key range split over CTAs with
-the partial results merged) and fa_fwd_block_sparse (128×128 blocks switched off).
+the partial results merged; Tq = 1 runs the CUDA-core decode kernel) and
+fa_fwd_block_sparse (128×128 blocks switched off).
 
 Tolerances as for the forward: O max-abs ≤ 2e-2, mean-abs ≤ 1e-3 (+ 2⁻⁹·mean|O_ref| for
 shapes whose rows see few keys, as in test_parity.py), LSE ≤ 1e-3 absolute on rows that see
@@ -42,6 +43,10 @@ def _qkv_kv(B, H, Tq, Tk, d, seed):
     (2, 12, 1, 4096, 64, True, 0),     # decode, automatic ranges
     (2, 12, 1, 4096, 64, True, 1),     # decode, one range
     (2, 12, 1, 4096, 64, True, 5),     # uneven ranges
+    (1, 3, 1, 1, 64, True, 0),         # decode against a single cached key
+    (1, 3, 1, 5, 128, True, 8),        # more ranges requested than keys
+    (2, 6, 1, 8192, 128, False, 3),
+    (1, 4, 1, 777, 64, True, 0),       # ragged cache length
     (1, 8, 1, 1000, 128, False, 0),
     (2, 4, 7, 2000, 64, True, 3),
     (1, 4, 128, 1024, 64, True, 0),
