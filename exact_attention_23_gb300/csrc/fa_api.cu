@@ -68,14 +68,15 @@ int check_device(int* dev_out, int* sms_out) {
 }
 
 // 3-D map over a [B·H][T][d] bf16 tensor: dim 0 = d (contiguous), dim 1 = T, dim 2 = B·H.
-// Boxes are 64 columns (128 bytes, the 128-byte swizzle span) × 128 rows × 1 head. Rows
-// past T read as zeros, so a ragged last tile never touches the next head.
-bool encode_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, int T, int d, int BH) {
+// Boxes are 64 columns (128 bytes, the 128-byte swizzle span) × box_rows rows × 1 head.
+// Rows past T read as zeros, so a ragged last tile never touches the next head.
+bool encode_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, int T, int d, int BH,
+                int box_rows) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(T),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(T) * static_cast<cuuint64_t>(d) * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t elem_strides[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
              elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

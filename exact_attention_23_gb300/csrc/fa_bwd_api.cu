@@ -19,7 +19,7 @@ extern "C" {
 // Workspace: [BH][T_pad] fp32 lse2, [BH][T_pad] fp32 D, [BH][T_pad][d] fp32 dQ accumulator,
 // each section starting on a 256-byte boundary. Returns 0 for unsupported sizes.
 size_t fa_bwd_workspace_size(int B, int H, int T, int d) {
-  if (B <= 0 || H <= 0 || T <= 0 || d != 64) return 0;
+  if (B <= 0 || H <= 0 || T <= 0 || (d != 64 && d != 128)) return 0;
   const long long BH = static_cast<long long>(B) * H;
   const long long T_pad = (static_cast<long long>(T) + 127) / 128 * 128;
   if (BH > INT32_MAX || T_pad > INT32_MAX || (T_pad / 128) * BH > INT32_MAX) return 0;
@@ -35,14 +35,16 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
               int* status, unsigned long long timeout_ns, unsigned int flags, void* stream) {
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
     return FA_ERR_INVALID_ARG;
-  if (B <= 0 || H <= 0 || T <= 0 || d != 64) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || T <= 0 || (d != 64 && d != 128)) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
   if ((flags & ~static_cast<unsigned>(FA_FLAG_TEST_STARVE_Q)) != 0u) return FA_ERR_INVALID_ARG;
   const size_t need = fa_bwd_workspace_size(B, H, T, d);
   if (need == 0 || workspace_bytes < need) return FA_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * H;
-  const long long n_qt = (static_cast<long long>(T) + 127) / 128;
-  const long long T_pad = n_qt * 128;
+  const long long n_kt = (static_cast<long long>(T) + 127) / 128;  // 128-key tiles
+  const long long T_pad = n_kt * 128;
+  const int bq = (d == 64) ? 128 : 64;                                // query tile rows
+  const long long n_qt = T_pad / bq;
   const long long elems = BH * T * d;
   if (elems >= (1LL << 62) / 2) return FA_ERR_INVALID_ARG;
   if (static_cast<long long>(T) * d * 2 >= (1LL << 40)) return FA_ERR_INVALID_ARG;
@@ -70,10 +72,10 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   if (!enc) return FA_ERR_LAUNCH;
 
   fa::BwdLaunch a;
-  if (!encode_map(enc, &a.tm_q, q, T, d, static_cast<int>(BH)) ||
+  if (!encode_map(enc, &a.tm_q, q, T, d, static_cast<int>(BH), bq) ||
       !encode_map(enc, &a.tm_k, k, T, d, static_cast<int>(BH)) ||
       !encode_map(enc, &a.tm_v, v, T, d, static_cast<int>(BH)) ||
-      !encode_map(enc, &a.tm_do, dout, T, d, static_cast<int>(BH)))
+      !encode_map(enc, &a.tm_do, dout, T, d, static_cast<int>(BH), bq))
     return FA_ERR_INVALID_ARG;
   auto up = [](size_t x) { return (x + 255u) / 256u * 256u; };
   const size_t rows = static_cast<size_t>(BH) * static_cast<size_t>(T_pad);
@@ -90,6 +92,7 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   a.p.T_pad = static_cast<int>(T_pad);
   a.p.BH = static_cast<int>(BH);
   a.p.n_qt = static_cast<int>(n_qt);
+  a.p.n_kt = static_cast<int>(n_kt);
   // Heads per group: Q and dO (bf16) plus the fp32 dQ accumulator are 8·T·d bytes per
   // head; about 64 MB of them (half the 129 MB L2) per group.
   const long long per_head = 8LL * T_pad * d;
@@ -102,12 +105,13 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   a.dout = static_cast<const __nv_bfloat16*>(dout);
   a.lse = lse;
   a.dq = static_cast<__nv_bfloat16*>(dq);
-  a.grid_main = static_cast<unsigned>(n_qt * BH);
+  a.grid_main = static_cast<unsigned>(n_kt * BH);
   // The two streaming kernels: a few resident blocks per SM, grid-stride loops.
   a.grid_prep = static_cast<unsigned>(sms) * 8u;
   a.grid_dq = static_cast<unsigned>(sms) * 8u;
   a.stream = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = fa::launch_bwd_d64(a, causal != 0);
+  const cudaError_t e =
+      (d == 64) ? fa::launch_bwd_d64(a, causal != 0) : fa::launch_bwd_d128(a, causal != 0);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 

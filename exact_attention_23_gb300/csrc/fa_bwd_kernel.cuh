@@ -58,23 +58,37 @@ constexpr int kBwdScoreWarp = 12;
 constexpr int kBwdGradWarp = 13;
 constexpr int kBwdLoadWarp = 14;
 
+// Tile shapes. Keys are always in 128-row tiles (the TMEM lanes of Sᵀ, dPᵀ, dV and dK).
+// Query tiles have kBQ rows: 128 at d = 64; 64 at d = 128, where 128-column Sᵀ, dPᵀ, dV and
+// dK would already fill the 512 TMEM columns. With 64-query tiles every product keeps
+// M = 128: dQ is then made transposed, dQᵀ = Kᵀ·dSᵀ (head dims on TMEM lanes, N = 64).
 template <int D>
 struct BwdCfg {
-  static_assert(D == 64, "the backward kernel is built for head dim 64");
-  static constexpr int kBox = 128 * 64 * 2;           // one 128-row × 64-col bf16 box = 16 KB
-  static constexpr int kTileBytes = 128 * D * 2;
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kBQ = (D == 64) ? 128 : 64;    // query rows per tile
+  static constexpr int kNC = kBQ / 2;                 // query columns per compute warpgroup
+  static constexpr int kBox = 128 * 64 * 2;           // 128 rows × 64 bf16 columns = 16 KB
+  static constexpr int kQBox = kBQ * 64 * 2;          // kBQ rows × 64 columns
+  static constexpr int kKVTile = 128 * D * 2;         // a K or V tile
+  static constexpr int kQTile = kBQ * D * 2;          // a Q or dO tile
   static constexpr int kK = 0;
-  static constexpr int kV = kK + kTileBytes;
+  static constexpr int kV = kK + kKVTile;
   static constexpr int kStages = 3;                   // (Q_i, dO_i) ring depth
-  static constexpr int kStage0 = kV + kTileBytes;     // stage s: Q at +0, dO at +kTileBytes
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kDS = kStage0 + kStages * kStageBytes;  // dSᵀ: 2 buffers × 2 boxes
-  static constexpr int kDSBytes = 2 * kBox;
-  static constexpr int kVec = kDS + 2 * kDSBytes;     // stage s: lse2[128] then D[128] (fp32)
-  static constexpr int kBar = kVec + kStages * 1024;
+  static constexpr int kStage0 = kV + kKVTile;        // stage s: Q at +0, dO at +kQTile
+  static constexpr int kStageBytes = 2 * kQTile;
+  static constexpr int kDS = kStage0 + kStages * kStageBytes;  // dSᵀ: 2 buffers
+  static constexpr int kDSBytes = 128 * kBQ * 2;      // [128 keys][kBQ queries] bf16, 64-col boxes
+  static constexpr int kVecBytes = 2 * kBQ * 4;       // per stage: lse2[kBQ] then D[kBQ]
+  static constexpr int kVec = kDS + 2 * kDSBytes;
+  static constexpr int kBar = kVec + kStages * kVecBytes;
   static constexpr int kSmemBytes = kBar + 256 + 1024;  // barriers + 1 KB alignment slack
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
-  static constexpr uint32_t kColDQ = 256 + 2 * D, kColP = 448;
+  // Tensor memory: Sᵀ, dPᵀ (kBQ columns each), dV, dK (D each), dQ (D columns at d = 64,
+  // dQᵀ with kBQ columns at d = 128), Pᵀ as bf16 pairs (kBQ/2 columns).
+  static constexpr uint32_t kColS = 0, kColDP = kBQ, kColDV = 2 * kBQ, kColDK = 2 * kBQ + D;
+  static constexpr uint32_t kColDQ = 2 * kBQ + 2 * D;
+  static constexpr uint32_t kColP = kColDQ + ((D == 64) ? D : kBQ);
+  static_assert(kColP + kBQ / 2 <= 512, "tensor memory");
+  static_assert(kSmemBytes <= 232448, "shared memory");
 };
 
 struct BwdBars {
@@ -104,12 +118,13 @@ struct BwdParams {
   __nv_bfloat16* dv;
   const float* lse2;   // [BH][T_pad] log2(e)·LSE, +∞ on padding rows
   const float* dvec;   // [BH][T_pad] D_i, 0 on padding rows
-  float* dq_acc;       // [BH][n_qt][D/4][128][4] fp32 dQ accumulator (unscaled)
+  float* dq_acc;       // fp32 dQ accumulator (unscaled), layout of dq_acc_offset
   int* status;
   int T;
-  int T_pad;           // n_qt · 128
+  int T_pad;           // ceil(T / 128) · 128
   int BH;
-  int n_qt;            // ceil(T / 128): query tiles = key tiles
+  int n_qt;            // T_pad / kBQ query tiles
+  int n_kt;            // T_pad / 128 key tiles
   int head_group;      // heads whose units are interleaved (see the unit order)
   float scale;
   float scale_log2;    // scale · log2(e)
@@ -119,12 +134,17 @@ struct BwdParams {
 
 constexpr uint32_t kBwdFlagStarveQ = 1u;  // FA_FLAG_TEST_STARVE_Q
 
-// Offset (in floats) of query row r, columns 4·c4 .. 4·c4+3 of tile (bh, i) in the dQ
-// accumulator. The layout puts the 128 rows of one 4-column group next to each other so
-// that a warp's 32 vector adds cover 512 contiguous bytes.
+// dQ accumulator layouts, chosen so that a warp's 32 vector adds cover 512 contiguous bytes.
+// d = 64 (thread = query row r of a 128-row tile): [bh][tile][d/4][128 rows][4 columns];
+//   dq_acc_offset(bh, i, n_qt, c4, r, d) is query row r, columns 4·c4 .. 4·c4+3.
+// d = 128 (dQᵀ: thread = head dim c of a 64-query tile): [bh][tile][16][128 dims][4 rows];
+//   dq_acc_offset_t(bh, i, n_qt, g, c) is head dim c of query rows 4·g .. 4·g+3.
 __host__ __device__ __forceinline__ size_t dq_acc_offset(int bh, int i, int n_qt, int c4, int r,
                                                          int d) {
   return ((((size_t)bh * n_qt + i) * (size_t)(d / 4) + c4) * 128u + r) * 4u;
+}
+__host__ __device__ __forceinline__ size_t dq_acc_offset_t(int bh, int i, int n_qt, int g, int c) {
+  return ((((size_t)bh * n_qt + i) * 16u + g) * 128u + c) * 4u;
 }
 
 // ------------------------------------------------------------------------------------
@@ -177,32 +197,67 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
 }
 
 // ------------------------------------------------------------------------------------
-// dQ = scale · accumulator, as bf16 rows. One thread per (tile, 8 columns, row).
+// dQ = scale · accumulator, as bf16 rows.
+// d = 64: one thread per (tile, 8 columns, row). d = 128: one thread per (64-row tile,
+// group of 4 rows, 8 head dims), writing 4 rows × 8 columns.
 // ------------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ dq_acc,
                                                         __nv_bfloat16* __restrict__ dq, int T,
                                                         int n_qt, int BH, float scale) {
   constexpr int C8 = D / 8;
-  const size_t total = (size_t)BH * n_qt * C8 * 128;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
-    const int r = static_cast<int>(idx % 128);
-    const size_t rest = idx / 128;
-    const int c8 = static_cast<int>(rest % C8);
-    const size_t tile = rest / C8;  // bh · n_qt + i
-    const int i = static_cast<int>(tile % n_qt);
-    const int bh = static_cast<int>(tile / n_qt);
-    const int t = i * 128 + r;
-    if (t >= T) continue;
-    const float4 a = *reinterpret_cast<const float4*>(dq_acc + dq_acc_offset(bh, i, n_qt, 2 * c8, r, D));
-    const float4 b = *reinterpret_cast<const float4*>(dq_acc + dq_acc_offset(bh, i, n_qt, 2 * c8 + 1, r, D));
-    uint4 out;
-    out.x = pack_bf16x2(a.x * scale, a.y * scale);
-    out.y = pack_bf16x2(a.z * scale, a.w * scale);
-    out.z = pack_bf16x2(b.x * scale, b.y * scale);
-    out.w = pack_bf16x2(b.z * scale, b.w * scale);
-    *reinterpret_cast<uint4*>(dq + ((size_t)bh * T + t) * D + (size_t)c8 * 8) = out;
+  if constexpr (D == 64) {
+    const size_t total = (size_t)BH * n_qt * C8 * 128;
+    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+      const int r = static_cast<int>(idx % 128);
+      const size_t rest = idx / 128;
+      const int c8 = static_cast<int>(rest % C8);
+      const size_t tile = rest / C8;  // bh · n_qt + i
+      const int i = static_cast<int>(tile % n_qt);
+      const int bh = static_cast<int>(tile / n_qt);
+      const int t = i * 128 + r;
+      if (t >= T) continue;
+      const float4 a = *reinterpret_cast<const float4*>(dq_acc + dq_acc_offset(bh, i, n_qt, 2 * c8, r, D));
+      const float4 b = *reinterpret_cast<const float4*>(dq_acc + dq_acc_offset(bh, i, n_qt, 2 * c8 + 1, r, D));
+      uint4 out;
+      out.x = pack_bf16x2(a.x * scale, a.y * scale);
+      out.y = pack_bf16x2(a.z * scale, a.w * scale);
+      out.z = pack_bf16x2(b.x * scale, b.y * scale);
+      out.w = pack_bf16x2(b.z * scale, b.w * scale);
+      *reinterpret_cast<uint4*>(dq + ((size_t)bh * T + t) * D + (size_t)c8 * 8) = out;
+    }
+  } else {
+    const size_t total = (size_t)BH * n_qt * 16 * C8;
+    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+      const int c8 = static_cast<int>(idx % C8);
+      const size_t rest = idx / C8;
+      const int g = static_cast<int>(rest % 16);
+      const size_t tile = rest / 16;
+      const int i = static_cast<int>(tile % n_qt);
+      const int bh = static_cast<int>(tile / n_qt);
+      float4 col[8];  // head dims c8·8 .. c8·8+7, each holding rows 4g .. 4g+3
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        col[e] = *reinterpret_cast<const float4*>(dq_acc + dq_acc_offset_t(bh, i, n_qt, g, c8 * 8 + e));
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int t = i * 64 + 4 * g + rr;
+        if (t >= T) break;
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 cv = col[e];
+          y[e] = (rr == 0 ? cv.x : rr == 1 ? cv.y : rr == 2 ? cv.z : cv.w) * scale;
+        }
+        uint4 out;
+        out.x = pack_bf16x2(y[0], y[1]);
+        out.y = pack_bf16x2(y[2], y[3]);
+        out.z = pack_bf16x2(y[4], y[5]);
+        out.w = pack_bf16x2(y[6], y[7]);
+        *reinterpret_cast<uint4*>(dq + ((size_t)bh * T + t) * D + (size_t)c8 * 8) = out;
+      }
+    }
   }
 }
 
@@ -230,14 +285,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // Unit order: heads in groups of head_group, small enough that a group's Q, dO and dQ
   // accumulator stay in L2 while its CTAs run; within a group, heaviest units first (under
-  // the causal mask key tile j sees n_qt − j query tiles), all heads at one j together.
-  const int per_group = p.head_group * p.n_qt;
+  // the causal mask key tile j sees the query tiles from the one holding query 128·j on),
+  // all heads at one j together.
+  const int per_group = p.head_group * p.n_kt;
   const int grp = blockIdx.x / per_group;
   const int within = blockIdx.x - grp * per_group;
   const int gsize = min(p.head_group, p.BH - grp * p.head_group);
   const int j = within / gsize;
   const int bh = grp * p.head_group + within % gsize;
-  const int i0 = CAUSAL ? j : 0;
+  const int i0 = CAUSAL ? (j * 128) / C::kBQ : 0;
   const int n = p.n_qt - i0;
 
   if (threadIdx.x == 0) {
@@ -276,13 +332,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const WaitCtl drain_wc{&bars->never, nullptr, p.timeout_ns};
   const uint32_t sbase = smem_u32(sm);
   auto q_s = [&](int st) { return sbase + C::kStage0 + st * C::kStageBytes; };
-  auto do_s = [&](int st) { return q_s(st) + C::kTileBytes; };
-  // Operand steps: K-major, 16 columns = 32 bytes inside a 64-column box, next box 16 KB
-  // on; MN-major, 16 rows = 2 KB, boxes along M/N 16 KB apart (leading byte offset).
-  auto kmaj = [&](uint32_t base, int kk) {
-    return sdesc_sw128(base + (kk >> 2) * C::kBox + (kk & 3) * 32, 16, 1024);
+  auto do_s = [&](int st) { return q_s(st) + C::kQTile; };
+  // Operand steps: K-major, 16 columns = 32 bytes inside a 64-column box, next box `box`
+  // bytes on; MN-major, 16 rows = 2 KB, boxes along M/N `box` bytes apart (leading byte
+  // offset). K/V tiles and dSᵀ have 128-row boxes (16 KB); Q/dO tiles kBQ-row boxes.
+  auto kmaj = [&](uint32_t base, int kk, uint32_t box) {
+    return sdesc_sw128(base + (kk >> 2) * box + (kk & 3) * 32, 16, 1024);
   };
-  auto mnmaj = [&](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, C::kBox, 1024); };
+  auto mnmaj = [&](uint32_t base, int kk, uint32_t box) {
+    return sdesc_sw128(base + kk * 2048, box, 1024);
+  };
   // End of every role (each calls it last, so that no code is shared between warpgroups
   // that run with different register budgets). Nothing may be in flight on the tensor
   // core when TMEM is released.
@@ -310,7 +369,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTileBytes);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kKVTile);
 #pragma unroll
       for (int b = 0; b < D / 64; ++b) {
         tma_load_3d(sm + C::kK + b * C::kBox, &tm_k, &bars->kv_full, b * 64, j * 128, bh);
@@ -325,17 +384,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) {
         const int i = i0 + t;
         uint8_t* stage = sm + C::kStage0 + st * C::kStageBytes;
-        float* vec = reinterpret_cast<float*>(sm + C::kVec + st * 1024);
-        mbar_arrive_expect_tx(&bars->q_full[st], 2 * C::kTileBytes + 1024);
+        float* vec = reinterpret_cast<float*>(sm + C::kVec + st * C::kVecBytes);
+        mbar_arrive_expect_tx(&bars->q_full[st], 2 * C::kQTile + C::kVecBytes);
 #pragma unroll
         for (int b = 0; b < D / 64; ++b) {
-          tma_load_3d(stage + b * C::kBox, &tm_q, &bars->q_full[st], b * 64, i * 128, bh);
-          tma_load_3d(stage + C::kTileBytes + b * C::kBox, &tm_do, &bars->q_full[st], b * 64,
-                      i * 128, bh);
+          tma_load_3d(stage + b * C::kQBox, &tm_q, &bars->q_full[st], b * 64, i * C::kBQ, bh);
+          tma_load_3d(stage + C::kQTile + b * C::kQBox, &tm_do, &bars->q_full[st], b * 64,
+                      i * C::kBQ, bh);
         }
-        const size_t row0 = (size_t)bh * p.T_pad + (size_t)i * 128;
-        bulk_load(vec, p.lse2 + row0, 512, &bars->q_full[st]);
-        bulk_load(vec + 128, p.dvec + row0, 512, &bars->q_full[st]);
+        const size_t row0 = (size_t)bh * p.T_pad + (size_t)i * C::kBQ;
+        bulk_load(vec, p.lse2 + row0, C::kBQ * 4, &bars->q_full[st]);
+        bulk_load(vec + C::kBQ, p.dvec + row0, C::kBQ * 4, &bars->q_full[st]);
       }
       last_t[st] = t;
       __syncwarp();
@@ -348,7 +407,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (last_t[s] >= 0) mbar_wait_warp_inl(&bars->q_full[s], (last_t[s] / NS) & 1, drain_wc);
   } else if (warp == kBwdScoreWarp) {
     // ---------------------------------------------------------------- score issuer
-    constexpr uint32_t kIdS = idesc_bf16(128, 128, false);  // Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ
+    constexpr uint32_t kIdS = idesc_bf16(128, C::kBQ, false);  // Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ
     const uint32_t k_s = sbase + C::kK, v_s = sbase + C::kV;
     bool ok = mbar_wait_warp_inl(&bars->kv_full, 0, wc);
     for (int t = 0, st = 0, ph = 0; t < n && ok; ++t) {
@@ -359,7 +418,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColS, kmaj(k_s, kk), kmaj(q_s(st), kk), kIdS, kk > 0);
+          mma_ss(tmem + C::kColS, kmaj(k_s, kk, C::kBox), kmaj(q_s(st), kk, C::kQBox), kIdS,
+                 kk > 0);
         mma_commit(&bars->s_full);
       }
       __syncwarp();
@@ -369,7 +429,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::kColDP, kmaj(v_s, kk), kmaj(do_s(st), kk), kIdS, kk > 0);
+          mma_ss(tmem + C::kColDP, kmaj(v_s, kk, C::kBox), kmaj(do_s(st), kk, C::kQBox), kIdS,
+                 kk > 0);
         mma_commit(&bars->dp_full);
         mma_commit(&bars->q_empty[st]);
       }
@@ -382,7 +443,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ---------------------------------------------------------------- gradient issuer
     constexpr uint32_t kIdV = idesc_bf16(128, D, true);             // dV: A in TMEM, B MN-major
     constexpr uint32_t kIdK = idesc_bf16_ab(128, D, false, true);   // dK: A K-major, B MN-major
-    constexpr uint32_t kIdQ = idesc_bf16_ab(128, D, true, true);    // dQ: A and B MN-major
+    // dQ (d = 64: dS·K, M = queries) or dQᵀ (d = 128: Kᵀ·dSᵀ, M = head dims): both operands
+    // MN-major, N = D or kBQ.
+    constexpr uint32_t kIdQ = idesc_bf16_ab(128, (D == 64) ? D : C::kBQ, true, true);
     const uint32_t k_s = sbase + C::kK;
     bool ok = true;
     for (int t = 0, st = 0; t < n && ok; ++t) {
@@ -392,13 +455,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after_sync();
       if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::kColDV, tmem + C::kColP + kk * 8, mnmaj(do_s(st), kk), kIdV,
+        for (int kk = 0; kk < C::kBQ / 16; ++kk)
+          mma_ts(tmem + C::kColDV, tmem + C::kColP + kk * 8, mnmaj(do_s(st), kk, C::kQBox), kIdV,
                  (t > 0 || kk > 0));
         mma_commit(&bars->p_free);
       }
       __syncwarp();
-      // dK += dSᵀ·Q_i, then dQ_i = dS·K_j
+      // dK += dSᵀ·Q_i, then dQ_i = dS·K_j (d = 64) or dQ_iᵀ = K_jᵀ·dSᵀ (d = 128)
       const int b = t & 1;
       const uint32_t ds_s = sbase + C::kDS + b * C::kDSBytes;
       if (!(ok = mbar_wait_warp_inl(&bars->ds_full[b], (t >> 1) & 1, wc))) break;
@@ -407,11 +470,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after_sync();
       if (lane == 0) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::kColDK, kmaj(ds_s, kk), mnmaj(q_s(st), kk), kIdK, (t > 0 || kk > 0));
+        for (int kk = 0; kk < C::kBQ / 16; ++kk)
+          mma_ss(tmem + C::kColDK, kmaj(ds_s, kk, C::kBox), mnmaj(q_s(st), kk, C::kQBox), kIdK,
+                 (t > 0 || kk > 0));
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + C::kColDQ, mnmaj(ds_s, kk), mnmaj(k_s, kk), kIdQ, kk > 0);
+        for (int kk = 0; kk < 8; ++kk) {  // K = 128 keys
+          if constexpr (D == 64)
+            mma_ss(tmem + C::kColDQ, mnmaj(ds_s, kk, C::kBox), mnmaj(k_s, kk, C::kBox), kIdQ, kk > 0);
+          else
+            mma_ss(tmem + C::kColDQ, mnmaj(k_s, kk, C::kBox), mnmaj(ds_s, kk, C::kBox), kIdQ, kk > 0);
+        }
         mma_commit(&bars->dq_full);
         mma_commit(&bars->ds_free[b]);
         mma_commit(&bars->q_empty[st]);
@@ -426,24 +494,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp >= kBwdDrainWarp0) {
     // ---------------------------------------------------------------- dQ drain
     const int qd = warp & 3;
-    const int r = qd * 32 + lane;  // query row within the tile = TMEM lane
+    // TMEM lane = query row (d = 64, dQ) or head dim (d = 128, dQᵀ); either way 64 columns
+    // and 16 vector adds of 4 values, 512 floats apart in the accumulator.
+    const int r = qd * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    auto acc_base = [&](int i) {
+      return p.dq_acc + ((D == 64) ? dq_acc_offset(bh, i, p.n_qt, 0, r, D)
+                                   : dq_acc_offset_t(bh, i, p.n_qt, 0, r));
+    };
     int t = 0;
     bool ok = true;
     for (; t < n; ++t) {
       if (!(ok = mbar_wait_warp_inl(&bars->dq_full, t & 1, wc))) break;
       FA_TRACE(20, t);
       tc_fence_after_sync();
-      float* dst = p.dq_acc + dq_acc_offset(bh, i0 + t, p.n_qt, 0, r, D);
-      // 32 columns at a time (the drain's register budget); the buffer is released once
-      // the last columns are in registers.
+      float* dst = acc_base(i0 + t);
+      // 32 columns at a time; the buffer is released once the last columns are in registers.
 #pragma unroll
-      for (int h = 0; h < D / 32; ++h) {
+      for (int h = 0; h < 2; ++h) {
         uint32_t x[32];
         tmem_ld32(tmem + lane_off + C::kColDQ + h * 32, x);
         tmem_ld_wait();
         reg_fence32(x);
-        if (h == D / 32 - 1) {
+        if (h == 1) {
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->dq_free);
@@ -460,58 +533,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // Abandoned tiles: poison their dQ rows so that the failure cannot go unseen.
       const float nan = __int_as_float(0x7fc00000);
       for (; t < n; ++t) {
-        float* dst = p.dq_acc + dq_acc_offset(bh, i0 + t, p.n_qt, 0, r, D);
-        for (int c4 = 0; c4 < D / 4; ++c4) red_add_v4(dst + (size_t)c4 * 512, nan, nan, nan, nan);
+        float* dst = acc_base(i0 + t);
+        for (int c4 = 0; c4 < 16; ++c4) red_add_v4(dst + (size_t)c4 * 512, nan, nan, nan, nan);
       }
     }
     teardown();
   } else {
     // ---------------------------------------------------------------- compute (warps 0-7)
-    const int g = warp >> 2;          // query half: columns 64g .. 64g+63 of each tile
+    constexpr int NC = C::kNC;        // query columns of this warpgroup per tile (64 or 32)
+    const int g = warp >> 2;          // columns NC·g .. NC·g + NC − 1 of each tile
     const int qd = warp & 3;
     const int r = qd * 32 + lane;     // key row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    // dSᵀ columns of this warpgroup: box (NC·g)/64, 16-byte chunks from ((NC·g) mod 64)/8
+    const int ds_box_idx = (NC * g) / 64, ds_chunk0 = ((NC * g) % 64) / 8;
     bool ok = true;
     for (int t = 0, st = 0, ph = 0; t < n && ok; ++t) {
       const int i = i0 + t;
-      const float* vec = reinterpret_cast<const float*>(sm + C::kVec + st * 1024);
+      const float* vec = reinterpret_cast<const float*>(sm + C::kVec + st * C::kVecBytes);
       if (!(ok = mbar_wait_warp_inl(&bars->q_full[st], ph, wc))) break;
       if (!(ok = mbar_wait_warp_inl(&bars->s_full, t & 1, wc))) break;
       FA_TRACE(10, t);
       tc_fence_after_sync();
-      uint32_t s[64];
-      tmem_ld32(tmem + lane_off + C::kColS + g * 64, s);
-      tmem_ld32(tmem + lane_off + C::kColS + g * 64 + 32, s + 32);
+      uint32_t s[NC];
+#pragma unroll
+      for (int h = 0; h < NC / 32; ++h) tmem_ld32(tmem + lane_off + C::kColS + g * NC + h * 32, s + h * 32);
       tmem_ld_wait();
-      reg_fence32(s);
-      reg_fence32(s + 32);
+#pragma unroll
+      for (int h = 0; h < NC / 32; ++h) reg_fence32(s + h * 32);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->s_free);
-      // Pᵀ = exp2(S·scale·log2e − lse2_q), zero above the diagonal (key > query)
-      float pr[64];
-      const float4* l4 = reinterpret_cast<const float4*>(vec + g * 64);
+      // Pᵀ = exp2(S·scale·log2e − lse2_q), zero where the key comes after the query
+      float pr[NC];
+      const float4* l4 = reinterpret_cast<const float4*>(vec + g * NC);
 #pragma unroll
-      for (int c = 0; c < 64; c += 4) {
+      for (int c = 0; c < NC; c += 4) {
         const float4 l = l4[c / 4];
         pr[c] = ex2_approx(fmaf(__uint_as_float(s[c]), p.scale_log2, -l.x));
         pr[c + 1] = ex2_approx(fmaf(__uint_as_float(s[c + 1]), p.scale_log2, -l.y));
         pr[c + 2] = ex2_approx(fmaf(__uint_as_float(s[c + 2]), p.scale_log2, -l.z));
         pr[c + 3] = ex2_approx(fmaf(__uint_as_float(s[c + 3]), p.scale_log2, -l.w));
       }
-      if (CAUSAL && i == j) {
+      if (CAUSAL && j * 128 + 127 > i * C::kBQ) {  // a tile the diagonal crosses
+        const int rel = j * 128 + r - (i * C::kBQ + g * NC);  // key − first query of the warpgroup
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (r > g * 64 + c) pr[c] = 0.f;
+        for (int c = 0; c < NC; ++c)
+          if (rel > c) pr[c] = 0.f;
       }
       FA_TRACE(11, t);
       if (t >= 1 && !(ok = mbar_wait_warp_inl(&bars->p_free, (t - 1) & 1, wc))) break;
       FA_TRACE(12, t);
-      uint32_t pk[32];
+      uint32_t pk[NC / 2];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+      for (int c = 0; c < NC / 2; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
       tc_fence_after_sync();
-      tmem_st32(tmem + lane_off + C::kColP + g * 32, pk);
+      if constexpr (NC == 64) tmem_st32(tmem + lane_off + C::kColP + g * 32, pk);
+      else tmem_st16(tmem + lane_off + C::kColP + g * 16, pk);
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
@@ -519,24 +597,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       FA_TRACE(13, t);
       // dSᵀ = Pᵀ ∘ (dPᵀ − D_q), into shared-memory buffer t mod 2
       const int b = t & 1;
-      const uint32_t ds_box = sbase + C::kDS + b * C::kDSBytes + g * C::kBox;
+      const uint32_t ds_box = sbase + C::kDS + b * C::kDSBytes + ds_box_idx * C::kBox;
       if (!(ok = mbar_wait_warp_inl(&bars->dp_full, t & 1, wc))) break;
       FA_TRACE(14, t);
       if (t >= 2 && !(ok = mbar_wait_warp_inl(&bars->ds_free[b], ((t >> 1) - 1) & 1, wc))) break;
       FA_TRACE(15, t);
       tc_fence_after_sync();
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < NC / 32; ++h) {
         uint32_t dp[32];
-        tmem_ld32(tmem + lane_off + C::kColDP + g * 64 + h * 32, dp);
+        tmem_ld32(tmem + lane_off + C::kColDP + g * NC + h * 32, dp);
         tmem_ld_wait();
         reg_fence32(dp);
-        if (h == 1) {
+        if (h == NC / 32 - 1) {
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->dp_free);
         }
-        const float4* d4 = reinterpret_cast<const float4*>(vec + 128 + g * 64 + h * 32);
+        const float4* d4 = reinterpret_cast<const float4*>(vec + C::kBQ + g * NC + h * 32);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           const float4 da = d4[2 * q4], db = d4[2 * q4 + 1];
@@ -551,7 +629,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ds[5] = pr[c + 5] * (__uint_as_float(dq8[5]) - db.y);
           ds[6] = pr[c + 6] * (__uint_as_float(dq8[6]) - db.z);
           ds[7] = pr[c + 7] * (__uint_as_float(dq8[7]) - db.w);
-          st_row_chunk_sw128(ds_box, r, h * 4 + q4, ds);
+          st_row_chunk_sw128(ds_box, r, ds_chunk0 + h * 4 + q4, ds);
         }
       }
       fence_proxy_async_smem();
@@ -560,33 +638,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       FA_TRACE(16, t);
       if (++st == NS) { st = 0; ph ^= 1; }
     }
-    // ---- epilogue: warpgroup 0 writes dV_j, warpgroup 1 writes scale·dK_j
-    const bool done = ok && mbar_wait_warp_inl(&bars->grad_done, 0, wc) && !bars->abort;
+    // ---- epilogue: warpgroup 0 writes dV_j, warpgroup 1 writes scale·dK_j (32 columns at
+    // a time)
+    bool done = ok && mbar_wait_warp_inl(&bars->grad_done, 0, wc) && !bars->abort;
+    done = __shfl_sync(0xffffffffu, done ? 1u : 0u, 0) != 0u;  // warp-uniform (TMEM loads)
     const int key = j * 128 + r;
     tc_fence_after_sync();
-    uint32_t x[D];
     const uint32_t col = (g == 0) ? C::kColDV : C::kColDK;
-#pragma unroll
-    for (int h = 0; h < D / 32; ++h)
-      if (done) tmem_ld32(tmem + lane_off + col + h * 32, x + h * 32);
-    if (done) tmem_ld_wait();
-#pragma unroll
-    for (int h = 0; h < D / 32; ++h) reg_fence32(x + h * 32);
     const float mul = (g == 0) ? 1.f : p.scale;
     const float nan = __int_as_float(0x7fc00000);
-    if (key < p.T) {
-      __nv_bfloat16* dst = ((g == 0) ? p.dv : p.dk) + ((size_t)bh * p.T + key) * D;
+    __nv_bfloat16* dst = ((g == 0) ? p.dv : p.dk) + ((size_t)bh * p.T + key) * D;
 #pragma unroll
-      for (int c = 0; c < D; c += 8) {
-        float y[8];
+    for (int h = 0; h < D / 32; ++h) {
+      uint32_t x[32];
+      if (done) {
+        tmem_ld32(tmem + lane_off + col + h * 32, x);
+        tmem_ld_wait();
+      }
+      reg_fence32(x);
+      if (key < p.T) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = done ? __uint_as_float(x[c + e]) * mul : nan;
-        uint4 v;
-        v.x = pack_bf16x2(y[0], y[1]);
-        v.y = pack_bf16x2(y[2], y[3]);
-        v.z = pack_bf16x2(y[4], y[5]);
-        v.w = pack_bf16x2(y[6], y[7]);
-        *reinterpret_cast<uint4*>(dst + c) = v;
+        for (int c = 0; c < 32; c += 8) {
+          float y[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = done ? __uint_as_float(x[c + e]) * mul : nan;
+          uint4 v;
+          v.x = pack_bf16x2(y[0], y[1]);
+          v.y = pack_bf16x2(y[2], y[3]);
+          v.z = pack_bf16x2(y[4], y[5]);
+          v.w = pack_bf16x2(y[6], y[7]);
+          *reinterpret_cast<uint4*>(dst + h * 32 + c) = v;
+        }
       }
     }
     teardown();

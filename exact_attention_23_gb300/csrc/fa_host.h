@@ -18,8 +18,9 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 EncodeTiledFn encode_fn();
 // FA_OK with the current device and its SM count if it is compute capability 10.3.
 int check_device(int* dev_out, int* sms_out);
-// 3-D map over a [B·H][T][d] bf16 tensor, boxes of 64 columns × 128 rows × 1 head.
-bool encode_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, int T, int d, int BH);
+// 3-D map over a [B·H][T][d] bf16 tensor, boxes of 64 columns × box_rows rows × 1 head.
+bool encode_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, int T, int d, int BH,
+                int box_rows = 128);
 bool overlaps(const void* a, size_t na, const void* b, size_t nb);
 bool aligned16(const void* p);
 

@@ -48,5 +48,6 @@ struct BwdLaunch {
 
 // Enqueues the three backward kernels (prep, main, dQ conversion) on a.stream.
 cudaError_t launch_bwd_d64(const BwdLaunch& a, bool causal);
+cudaError_t launch_bwd_d128(const BwdLaunch& a, bool causal);
 
 }  // namespace fa

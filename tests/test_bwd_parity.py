@@ -104,6 +104,14 @@ def test_bwd_parity_ragged_lengths(T, causal):
     _full_check(inputs.Workload(f"bwd_edge_t{T}", 1, 3, T, 64, causal, 2000 + T))
 
 
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 127, 128, 129, 200, 256, 385, 777, 1024])
+@pytest.mark.parametrize("causal", [True, False])
+def test_bwd_parity_d128(T, causal):
+    """Head dim 128 (64-query tiles, dQ made transposed): lengths around the 64-row query
+    tiles and the 128-row key tiles."""
+    _full_check(inputs.Workload(f"bwd_d128_t{T}", 2, 2, T, 128, causal, 3000 + T))
+
+
 def _sample(T, rng, n_random=24):
     fixed = [0, 1, 127, 128, 129, T // 2, T - 129, T - 128, T - 2, T - 1]
     s = set(r for r in fixed if 0 <= r < T)
@@ -145,6 +153,11 @@ def test_bwd_parity_sweep_sampled(T):
 def test_bwd_parity_non_causal_long_sampled():
     w = inputs.Workload("bwd_noncausal_t4096", 2, 4, 4096, 64, False, 31)
     _sampled_check(w)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_bwd_parity_d128_long_sampled(causal):
+    _sampled_check(inputs.Workload("bwd_d128_t8192", 2, 8, 8192, 128, causal, 32))
 
 
 def test_bwd_workspace_reuse_and_determinism():
@@ -199,5 +212,5 @@ def test_bwd_rejects_bad_workspace():
         fa.bwd(x, x.clone(), x.clone(), x.clone(), lse, x.clone(), workspace=small)
     assert e.value.status == fa.FA_ERR_INVALID_ARG
     with pytest.raises(fa.FAError):
-        y = torch.zeros(1, 2, 256, 128, dtype=torch.bfloat16, device="cuda")
+        y = torch.zeros(1, 2, 256, 96, dtype=torch.bfloat16, device="cuda")
         fa.bwd(y, y.clone(), y.clone(), y.clone(), lse, y.clone())

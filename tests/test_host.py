@@ -135,7 +135,8 @@ def test_bwd_workspace_size(lib):
     assert fa.fa_bwd_workspace_size(2, 3, 129, 64) == 2 * 6 * 256 * 4 + 6 * 256 * 64 * 4
     assert fa.fa_bwd_workspace_size(4, 12, 16384, 64) == 48 * 16384 * (2 + 64) * 4
     assert fa.fa_bwd_workspace_size(1, 1, 1, 64) == 2 * 512 + 128 * 64 * 4
-    for bad in ((0, 1, 128, 64), (1, 0, 128, 64), (1, 1, 0, 64), (1, 1, 128, 128),
+    assert fa.fa_bwd_workspace_size(1, 1, 128, 128) == 2 * 512 + 128 * 128 * 4
+    for bad in ((0, 1, 128, 64), (1, 0, 128, 64), (1, 1, 0, 64), (1, 1, 128, 96),
                 (1, 1, 128, 32), (1 << 16, 1 << 15, 1 << 16, 64)):
         assert fa.fa_bwd_workspace_size(*bad) == 0, bad
 
@@ -157,7 +158,7 @@ def _bwd_call(q=A, k=A + SZ, v=A + 2 * SZ, o=A + 3 * SZ, do=A + 4 * SZ, lse=A + 
     (dict(dq=0), fa.FA_ERR_INVALID_ARG),
     (dict(ws=0), fa.FA_ERR_INVALID_ARG),
     (dict(T=0), fa.FA_ERR_INVALID_ARG),
-    (dict(d=128), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(flags=4), fa.FA_ERR_INVALID_ARG),
     (dict(ws_bytes=1024), fa.FA_ERR_INVALID_ARG),                   # workspace too small
