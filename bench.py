@@ -313,6 +313,30 @@ def _time_calls(fn, steps, warmup, stream, torch, ws):
     return _max_over_ranks(a.elapsed_time(b), ws) / steps
 
 
+def _bwd_d128(args, fa, inputs, torch, dev, stream, bf16_sus, ws):
+    """Backward at head dim 128 on the wide-head workload (B2 H16 T16384, causal)."""
+    Bw, Hw, Tw, Dw = 2, 16, 16384, 128
+    q, k, v = (t.to(dev) for t in inputs.make_qkv(Bw, Hw, Tw, Dw, seed=10))
+    do = inputs.make_do(Bw, Hw, Tw, Dw, seed=10).to(dev)
+    o, lse = fa.fwd(q, k, v, causal=True)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    wsb = fa.bwd_workspace(Bw, Hw, Tw, Dw, device=dev)
+    scale = Dw ** -0.5
+
+    def call():
+        rc = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), wsb.data_ptr(),
+                       wsb.numel(), Bw, Hw, Tw, Dw, 1, scale, stream.cuda_stream)
+        if rc != fa.FA_OK:
+            raise fa.FAError(rc, "fa_bwd")
+    steps = max(1, min(args.steps, 20))
+    ms = _time_calls(call, steps, args.warmup, stream, torch, ws)
+    tf = ws * fa.bwd_flops(Bw, Hw, Tw, Dw, True) / ms / 1e9
+    return {"workload": "causal attention backward, bf16, B2 H16 T16384 d128", "value": tf,
+            "unit": "TFLOP/s", "ms_per_call": ms, "steps": steps,
+            "frac_of_sustained": tf / ws / bf16_sus, "gpu_launches": 3 * steps}
+
+
 def _general_forms(args, fa, inputs, torch, dev, stream, bf16_sus, hbm_peak, ws):
     """Decode (one new query per head against a 16k-token KV cache, B4 H12 d64, key range
     split over CTAs) and block-sparse self-attention (T = 8192, half of the 128×128 blocks
@@ -503,6 +527,8 @@ def run_gpu(args):
                        "frac_of_sustained": fl / ms / 1e9 / bf16_sus})
     bdom = max(bper_T, key=lambda r: r["T"])
     del bsets
+    # head dim 128 (64-query tiles): the wide-head workload, B2 H16 T16384
+    b128 = _bwd_d128(args, fa, inputs, torch, dev, stream, bf16_sus, ws)
 
     # ---- general forms: decode against a KV cache (split key ranges), block-sparse
     extra = _general_forms(args, fa, inputs, torch, dev, stream, bf16_sus, hbm_peak, ws)
@@ -588,6 +614,7 @@ def run_gpu(args):
                                        f"{fa.bwd_flops(B, H, bdom['T'], D, True):.4g} FLOP; peak = "
                                        f"{peak_kind} sustained bf16"},
                 "gpu_launches": 3 * args.steps * len(sweep),
+                "d128": b128,
                 "clocks": bclocks,
                 "cpu_baseline": bcpu,
             },
