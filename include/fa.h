@@ -165,7 +165,7 @@ int fa_fwd_block_sparse(const void* q, const void* k, const void* v, void* o, fl
 /*
  * fa_bwd_workspace_size — bytes of device workspace that fa_bwd needs for these sizes
  * (fp32 row statistics and an fp32 dQ accumulator: about B·H·T·(d + 2)·4 bytes).
- * Returns 0 when the sizes are not supported by fa_bwd (currently d must be 64).
+ * Returns 0 when the sizes are not supported by fa_bwd (d must be 64 or 128).
  */
 size_t fa_bwd_workspace_size(int B, int H, int T, int d);
 
@@ -183,7 +183,7 @@ size_t fa_bwd_workspace_size(int B, int H, int T, int d);
  *               run at the same time.
  *   causal, scale, stream : as for fa_fwd, and equal to the values of the forward call.
  *
- * Supported: d = 64; otherwise as fa_fwd. dq, dk, dv and the workspace must not overlap
+ * Supported: d ∈ {64, 128}; otherwise as fa_fwd. dq, dk, dv and the workspace must not overlap
  * any input or one another. The call enqueues three kernels on `stream` and returns; the
  * library allocates nothing. Returns FA_OK or an fa_status code (host-side validation
  * as for fa_fwd; nothing is launched on failure).
