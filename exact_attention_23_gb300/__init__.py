@@ -5,9 +5,10 @@
 per-row natural-log logsumexp in fp32. ``fwd_kv`` attends Tq queries to Tk ≥ Tq keys
 (bottom-right causal; key range split over CTAs when that fills the GPU), and
 ``fwd_block_sparse`` skips 128×128 blocks switched off by a block mask.
-``bwd(q, k, v, o, lse, do, causal)`` returns the gradients (dq, dk, dv) (d = 64 or 128). The work is done by the CUDA kernels of ``libfa.so``
-through its C ABI (include/fa.h); this module only allocates outputs and workspace with
-PyTorch and passes pointers and the current stream.
+``bwd(q, k, v, o, lse, do, causal)`` returns the gradients (dq, dk, dv) (d = 64 or 128).
+The work is done by the CUDA kernels of ``libfa.so`` through its C ABI (include/fa.h);
+this module only allocates outputs and workspace with PyTorch and passes pointers and the
+current stream.
 """
 
 from __future__ import annotations
