@@ -12,7 +12,8 @@ L2: each step touches ~0.8 GB of distinct inputs and outputs (more than 6× the 
 so every launch reads inputs last touched a full step earlier.
 
 The same line carries `decode` (one query per head against a 16k-token KV cache, GB/s),
-`block_sparse` (T = 8192 with half the 128×128 blocks kept, TFLOP/s on kept blocks) and a
+`block_sparse` (T = 8192 with half the 128×128 blocks kept, TFLOP/s on kept blocks),
+`fp8_qk` (e4m3 queries and keys, bf16 values, B2 H16 T16384 d128, causal) and a
 `backward` object: the gradient pass (dQ, dK, dV through fa_bwd)
 timed the same way over the same sweep, K steps, with an upstream gradient dO drawn per T;
 FLOPs are 2.5× the forward's (five T×T×d products instead of two).
@@ -337,6 +338,48 @@ def _bwd_d128(args, fa, inputs, torch, dev, stream, bf16_sus, ws):
             "frac_of_sustained": tf / ws / bf16_sus, "gpu_launches": 3 * steps}
 
 
+def _fwd_fp8(args, fa, inputs, torch, dev, stream, bf16_sus, ws):
+    """Forward with e4m3 Q/K codes (per-tensor scales) and bf16 V on the wide-head workload
+    (B2 H16 T16384 d128, causal), with the bf16 forward on the same values beside it. Q·Kᵀ
+    runs on the 8-bit tensor path (nominally 2x bf16) and P·V on the bf16 one, so the peak
+    for the mix is 2/(1/(2·P) + 1/P) = 4/3·P for the sustained bf16 peak P."""
+    Bw, Hw, Tw, Dw = 2, 16, 16384, 128
+    q8, sq, k8, sk, v = inputs.make_qk_fp8(Bw, Hw, Tw, Dw, seed=30)
+    q8, k8, v = q8.to(dev), k8.to(dev), v.to(dev)
+    qb = q8.view(torch.float8_e4m3fn).to(torch.bfloat16)
+    kb = k8.view(torch.float8_e4m3fn).to(torch.bfloat16)
+    o = torch.empty_like(v)
+    lse = torch.empty((Bw, Hw, Tw), dtype=torch.float32, device=dev)
+    scale = Dw ** -0.5
+
+    def call8():
+        rc = fa.fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), sq, sk, Bw, Hw, Tw, Dw, 1, scale, stream.cuda_stream)
+        if rc != fa.FA_OK:
+            raise fa.FAError(rc, "fa_fwd_fp8")
+
+    def call16():
+        rc = fa.fa_fwd(qb.data_ptr(), kb.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                       Bw, Hw, Tw, Dw, 1, scale * sq * sk, stream.cuda_stream)
+        if rc != fa.FA_OK:
+            raise fa.FAError(rc, "fa_fwd")
+    steps = max(1, min(args.steps, 20))
+    fl = fa.flops(Bw, Hw, Tw, Dw, True)
+    ms8 = _time_calls(call8, steps, args.warmup, stream, torch, ws)
+    ms16 = _time_calls(call16, steps, args.warmup, stream, torch, ws)
+    tf8, tf16 = ws * fl / ms8 / 1e9, ws * fl / ms16 / 1e9
+    peak = 4.0 / 3.0 * bf16_sus
+    return {"workload": "causal attention forward, e4m3 Q/K (per-tensor scales), bf16 V, "
+                        "B2 H16 T16384 d128",
+            "value": tf8, "unit": "TFLOP/s", "ms_per_call": ms8, "steps": steps,
+            "bf16_same_values": {"value": tf16, "unit": "TFLOP/s", "ms_per_call": ms16},
+            "roofline": {"bound": "tensor", "achieved": tf8 / ws, "peak": peak,
+                         "unit": "TFLOP/s", "frac": tf8 / ws / peak, "traffic": None,
+                         "peak_basis": "4/3 x sustained bf16 of measured (Q·Kᵀ at the "
+                                       "nominal 2x 8-bit rate, P·V at bf16)"},
+            "gpu_launches": 2 * steps}
+
+
 def _general_forms(args, fa, inputs, torch, dev, stream, bf16_sus, hbm_peak, ws):
     """Decode (one new query per head against a 16k-token KV cache, B4 H12 d64, key range
     split over CTAs) and block-sparse self-attention (T = 8192, half of the 128×128 blocks
@@ -532,6 +575,8 @@ def run_gpu(args):
 
     # ---- general forms: decode against a KV cache (split key ranges), block-sparse
     extra = _general_forms(args, fa, inputs, torch, dev, stream, bf16_sus, hbm_peak, ws)
+    # ---- FP8 (e4m3) queries and keys at head dim 128
+    extra["fp8_qk"] = _fwd_fp8(args, fa, inputs, torch, dev, stream, bf16_sus, ws)
 
     # ---- end to end: pinned host inputs -> device -> forward -> host, per step
     e2e_steps = max(1, min(args.steps, 10))

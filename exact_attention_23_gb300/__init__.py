@@ -31,6 +31,7 @@ from ._binding import (  # noqa: F401
     fa_fwd,
     fa_fwd_block_sparse,
     fa_fwd_ex,
+    fa_fwd_fp8,
     fa_fwd_kv,
     fa_fwd_kv_workspace_size,
     lib,
@@ -81,6 +82,33 @@ def fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=
                        stream)
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd")
+    return out, lse
+
+
+def fwd_fp8(q8, q_scale: float, k8, k_scale: float, v, causal: bool = True,
+            scale: float | None = None, out=None, lse=None):
+    """Forward with e4m3 query/key codes (CUDA uint8 tensors [B, H, T, d]) and their
+    per-tensor scales, bf16 v, through fa_fwd_fp8. Returns (o, lse)."""
+    import torch
+    for t, n in ((q8, "q8"), (k8, "k8")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.uint8 \
+                or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CUDA uint8 [B, H, T, d] tensor")
+    _check(v, "v")
+    if q8.shape != k8.shape or q8.shape != v.shape:
+        raise ValueError("q8, k8 and v must have the same shape")
+    B, H, T, d = v.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(v) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=v.device)
+    stream = torch.cuda.current_stream(v.device).cuda_stream
+    with torch.cuda.device(v.device):
+        rc = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v.data_ptr(), out.data_ptr(),
+                        lse.data_ptr(), q_scale, k_scale, B, H, T, d, causal, scale, stream)
+    if rc != FA_OK:
+        raise FAError(rc, "fa_fwd_fp8")
     return out, lse
 
 

@@ -96,6 +96,101 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 using namespace fa::host;
 
+namespace {
+
+// 3-D map over [B·H][T][d] e4m3 codes (one byte each): one box of d bytes × 128 rows × 1
+// head, swizzled in 128-byte (d = 128) or 64-byte (d = 64) rows.
+bool encode_map_e4m3(EncodeTiledFn enc, CUtensorMap* map, const void* base, int T, int d,
+                     int BH) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(T),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d),
+                                 static_cast<cuuint64_t>(T) * static_cast<cuuint64_t>(d)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 128, 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+             elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Validation, tensor maps and launch of the dense forward; qk8: q and k are e4m3 codes.
+int dense_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                  int T, int d, int causal, float scale_log2, int* status,
+                  unsigned long long timeout_ns, unsigned int flags, void* stream, bool qk8) {
+  // ---- host-side validation: nothing is launched on failure
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || T <= 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale_log2) || !(scale_log2 > 0.0f)) return FA_ERR_INVALID_ARG;
+  if ((flags & ~static_cast<unsigned>(FA_FLAG_TEST_STARVE_Q)) != 0u) return FA_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long n_qt = (static_cast<long long>(T) + 127) / 128;
+  const long long n_pairs = (n_qt + 1) / 2;
+  if (BH > INT32_MAX || n_qt * BH > INT32_MAX) return FA_ERR_INVALID_ARG;
+  const long long elems = BH * T * d;
+  if (elems >= (1LL << 62) / 2) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(T) * d * 2 >= (1LL << 40)) return FA_ERR_INVALID_ARG;  // TMA stride limit
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  const size_t tbytes = static_cast<size_t>(elems) * 2;
+  const size_t qkbytes = qk8 ? static_cast<size_t>(elems) : tbytes;
+  const size_t lbytes = static_cast<size_t>(BH) * T * 4;
+  if (overlaps(o, tbytes, q, qkbytes) || overlaps(o, tbytes, k, qkbytes) ||
+      overlaps(o, tbytes, v, tbytes) || overlaps(lse, lbytes, q, qkbytes) ||
+      overlaps(lse, lbytes, k, qkbytes) || overlaps(lse, lbytes, v, tbytes) ||
+      overlaps(lse, lbytes, o, tbytes))
+    return FA_ERR_INVALID_ARG;
+
+  int dev = -1, sms = 0;
+  const int dst = check_device(&dev, &sms);
+  if (dst != FA_OK) return dst;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return FA_ERR_LAUNCH;
+
+  fa::FwdLaunch a;
+  a.p = fa::FwdParams{};  // the general-form fields stay zero on this path
+  const bool maps_ok =
+      qk8 ? (encode_map_e4m3(enc, &a.tm_q, q, T, d, static_cast<int>(BH)) &&
+             encode_map_e4m3(enc, &a.tm_k, k, T, d, static_cast<int>(BH)))
+          : (encode_map(enc, &a.tm_q, q, T, d, static_cast<int>(BH)) &&
+             encode_map(enc, &a.tm_k, k, T, d, static_cast<int>(BH)));
+  if (!maps_ok || !encode_map(enc, &a.tm_v, v, T, d, static_cast<int>(BH)))
+    return FA_ERR_INVALID_ARG;
+  a.p.o = static_cast<__nv_bfloat16*>(o);
+  a.p.lse = lse;
+  a.p.status = status;
+  a.p.T = T;
+  a.p.BH = static_cast<int>(BH);
+  // Two 128-row Q tiles per CTA let the softmax of one overlap the MMAs of the other;
+  // only when pairs would leave most SMs idle does one tile per CTA pay.
+  const int tiles = (n_pairs * BH * 2 < sms) ? 1 : 2;
+  const long long n_units = (tiles == 2) ? n_pairs : n_qt;
+  a.p.n_units = static_cast<int>(n_units);
+  a.p.total_units = static_cast<int>(n_units * BH);
+  // All heads interleaved in one cost-sorted list. (Limiting the interleave to the heads
+  // whose K/V fit in L2 cut DRAM reads 2.6x at T = 16384 but measured 7-8 % slower: the
+  // re-reads cost no time at < 20 % of HBM bandwidth, the coarser balance did.)
+  a.p.head_group = static_cast<int>(BH);
+  a.p.tiles_per_cta = tiles;
+  a.p.n_kv = static_cast<int>(n_qt);
+  a.p.scale_log2 = scale_log2;
+  a.p.timeout_ns = timeout_ns ? timeout_ns : 2000000000ull;
+  a.p.flags = flags;
+  // Persistent: one CTA per SM (at most one per unit); each walks units blockIdx.x,
+  // blockIdx.x + gridDim.x, ...
+  a.grid = static_cast<unsigned>(std::min<long long>(n_units * BH, sms));
+  a.stream = static_cast<cudaStream_t>(stream);
+
+  const cudaError_t e = qk8 ? fa::launch_fwd_fp8(a, d, causal != 0)
+                            : (d == 64) ? fa::launch_fwd_d64(a, causal != 0)
+                                        : fa::launch_fwd_d128(a, causal != 0);
+  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* fa_version(void) { return "fa-gb300 0.1.0 sm_103a"; }
@@ -115,69 +210,19 @@ const char* fa_strerror(int status) {
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
               int T, int d, int causal, float scale, int* status, unsigned long long timeout_ns,
               unsigned int flags, void* stream) {
-  // ---- host-side validation: nothing is launched on failure
-  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-  if (B <= 0 || H <= 0 || T <= 0) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
-  if ((flags & ~static_cast<unsigned>(FA_FLAG_TEST_STARVE_Q)) != 0u) return FA_ERR_INVALID_ARG;
-  const long long BH = static_cast<long long>(B) * H;
-  const long long n_qt = (static_cast<long long>(T) + 127) / 128;
-  const long long n_pairs = (n_qt + 1) / 2;
-  if (BH > INT32_MAX || n_qt * BH > INT32_MAX) return FA_ERR_INVALID_ARG;
-  const long long elems = BH * T * d;
-  if (elems >= (1LL << 62) / 2) return FA_ERR_INVALID_ARG;
-  if (static_cast<long long>(T) * d * 2 >= (1LL << 40)) return FA_ERR_INVALID_ARG;  // TMA stride limit
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-    return FA_ERR_MISALIGNED;
-  const size_t tbytes = static_cast<size_t>(elems) * 2;
-  const size_t lbytes = static_cast<size_t>(BH) * T * 4;
-  if (overlaps(o, tbytes, q, tbytes) || overlaps(o, tbytes, k, tbytes) ||
-      overlaps(o, tbytes, v, tbytes) || overlaps(lse, lbytes, q, tbytes) ||
-      overlaps(lse, lbytes, k, tbytes) || overlaps(lse, lbytes, v, tbytes) ||
-      overlaps(lse, lbytes, o, tbytes))
-    return FA_ERR_INVALID_ARG;
+  return dense_forward(q, k, v, o, lse, B, H, T, d, causal,
+                       static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074),
+                       status, timeout_ns, flags, stream, false);
+}
 
-  int dev = -1, sms = 0;
-  const int dst = check_device(&dev, &sms);
-  if (dst != FA_OK) return dst;
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return FA_ERR_LAUNCH;
-
-  fa::FwdLaunch a;
-  a.p = fa::FwdParams{};  // the general-form fields stay zero on this path
-  if (!encode_map(enc, &a.tm_q, q, T, d, static_cast<int>(BH)) ||
-      !encode_map(enc, &a.tm_k, k, T, d, static_cast<int>(BH)) ||
-      !encode_map(enc, &a.tm_v, v, T, d, static_cast<int>(BH)))
-    return FA_ERR_INVALID_ARG;
-  a.p.o = static_cast<__nv_bfloat16*>(o);
-  a.p.lse = lse;
-  a.p.status = status;
-  a.p.T = T;
-  a.p.BH = static_cast<int>(BH);
-  // Two 128-row Q tiles per CTA let the softmax of one overlap the MMAs of the other;
-  // only when pairs would leave most SMs idle does one tile per CTA pay.
-  const int tiles = (n_pairs * BH * 2 < sms) ? 1 : 2;
-  const long long n_units = (tiles == 2) ? n_pairs : n_qt;
-  a.p.n_units = static_cast<int>(n_units);
-  a.p.total_units = static_cast<int>(n_units * BH);
-  // All heads interleaved in one cost-sorted list. (Limiting the interleave to the heads
-  // whose K/V fit in L2 cut DRAM reads 2.6x at T = 16384 but measured 7-8 % slower: the
-  // re-reads cost no time at < 20 % of HBM bandwidth, the coarser balance did.)
-  a.p.head_group = static_cast<int>(BH);
-  a.p.tiles_per_cta = tiles;
-  a.p.n_kv = static_cast<int>(n_qt);
-  a.p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-  a.p.timeout_ns = timeout_ns ? timeout_ns : 2000000000ull;
-  a.p.flags = flags;
-  // Persistent: one CTA per SM (at most one per unit); each walks units blockIdx.x,
-  // blockIdx.x + gridDim.x, ...
-  a.grid = static_cast<unsigned>(std::min<long long>(n_units * BH, sms));
-  a.stream = static_cast<cudaStream_t>(stream);
-
-  const cudaError_t e =
-      (d == 64) ? fa::launch_fwd_d64(a, causal != 0) : fa::launch_fwd_d128(a, causal != 0);
-  return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v, void* o, float* lse, float q_scale,
+               float k_scale, int B, int H, int T, int d, int causal, float scale, void* stream) {
+  for (float x : {q_scale, k_scale, scale})
+    if (!std::isfinite(x) || !(x > 0.0f)) return FA_ERR_INVALID_ARG;
+  const double sl2 = static_cast<double>(scale) * q_scale * k_scale * 1.4426950408889634074;
+  return dense_forward(q8, k8, v, o, lse, B, H, T, d, causal, static_cast<float>(sl2), nullptr,
+                       0ull, 0u, stream, true);
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int T,

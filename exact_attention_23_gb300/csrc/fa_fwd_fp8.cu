@@ -1,0 +1,31 @@
+// Instantiations of the attention forward with e4m3 Q and K (head dims 64 and 128).
+#include <atomic>
+
+#include "fa_launch.h"
+
+namespace fa {
+
+template <int D, bool CAUSAL>
+static cudaError_t launch_fp8(const FwdLaunch& a) {
+  auto* fn = &fa_fwd_kernel<D, CAUSAL, false, true>;
+  const int smem = Cfg<D, true>::kSmemBytes;
+  // The shared-memory opt-in is a per-device attribute: set it once per device.
+  static std::atomic<uint64_t> done[kMaxDevices / 64 + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const uint64_t bit = 1ull << (dev % 64);
+  if (!(done[dev / 64].load(std::memory_order_acquire) & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    done[dev / 64].fetch_or(bit, std::memory_order_acq_rel);
+  }
+  fn<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_fp8(const FwdLaunch& a, int d, bool causal) {
+  if (d == 64) return causal ? launch_fp8<64, true>(a) : launch_fp8<64, false>(a);
+  return causal ? launch_fp8<128, true>(a) : launch_fp8<128, false>(a);
+}
+
+}  // namespace fa

@@ -53,7 +53,7 @@ constexpr int kThreads = 352;
 constexpr float kTau = 8.0f;    // lazy rescale: O and l keep a stale max until it is 2^8 too small
 constexpr uint32_t kFlagStarveQ = 1u;  // FA_FLAG_TEST_STARVE_Q
 
-template <int D>
+template <int D, bool QK8 = false>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kStages = (D == 64) ? 3 : 2;      // K/V ring depth (measured: 3 beats 2, 4 and 6 at d=64)
@@ -61,9 +61,14 @@ struct Cfg {
   static constexpr int kSubBytes = kBlockM * 64 * 2;     // one 128-row × 64-col bf16 box = 16 KB
   static constexpr int kSub = D / 64;                    // boxes per tile row-block
   static constexpr int kTileBytes = kSub * kSubBytes;    // a 128×D bf16 tile
+  // Q and K tiles: bf16 as above, or (QK8) one box of 128 rows × D one-byte e4m3 codes,
+  // swizzled in 128-byte (D = 128) or 64-byte (D = 64) rows.
+  static constexpr int kQKSub = QK8 ? 1 : kSub;
+  static constexpr int kQKSubBytes = QK8 ? kBlockM * D : kSubBytes;
+  static constexpr int kQKTileBytes = kQKSub * kQKSubBytes;
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + kQBufs * 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kKOff = kQOff + kQBufs * 2 * kQKTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kQKTileBytes;
   static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + 1 KB alignment slack
   // Tensor-memory columns (see the layout at the top of this file).
@@ -223,11 +228,13 @@ __device__ __forceinline__ bool tile_active(const FwdParams& p, const Unit& u, i
   else return gen_active<CAUSAL>(p, u, i, kt);
 }
 
-template <int D, bool CAUSAL, bool GEN = false>
+// QK8: Q and K arrive as e4m3 codes (their per-tensor scales folded into scale_log2) and
+// S = Q·Kᵀ runs as a kind::f8f6f4 product; V, P and O are as in the bf16 path.
+template <int D, bool CAUSAL, bool GEN = false, bool QK8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, QK8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOff);
@@ -295,11 +302,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (qn >= C::kQBufs &&
           !mbar_wait_warp(&bars->q_empty[qb], ((qn / C::kQBufs) - 1) & 1, wc)) { ok = false; break; }
       if (load_q && leader) {
-        mbar_arrive_expect_tx(&bars->q_full[qb], p.tiles_per_cta * C::kTileBytes);
+        mbar_arrive_expect_tx(&bars->q_full[qb], p.tiles_per_cta * C::kQKTileBytes);
         for (int i = 0; i < p.tiles_per_cta; ++i)
 #pragma unroll
-          for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d(smem + C::kQOff + (qb * 2 + i) * C::kTileBytes + s * C::kSubBytes, &tm_q,
+          for (int s = 0; s < C::kQKSub; ++s)
+            tma_load_3d(smem + C::kQOff + (qb * 2 + i) * C::kQKTileBytes + s * C::kQKSubBytes, &tm_q,
                         &bars->q_full[qb], s * 64, (u.qt0 + i) * kBlockM, u.bh);
       }
       __syncwarp();
@@ -312,10 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (use > 0 && !mbar_wait_warp(&bars->kv_empty[st], (use - 1) & 1, wc)) { ok = false; break; }
         FA_TRACE(1, j);
         if (leader) {
-          mbar_arrive_expect_tx(&bars->k_full[st], C::kTileBytes);
+          mbar_arrive_expect_tx(&bars->k_full[st], C::kQKTileBytes);
 #pragma unroll
-          for (int s = 0; s < C::kSub; ++s)
-            tma_load_3d_hint(smem + C::kKOff + st * C::kTileBytes + s * C::kSubBytes, &tm_k,
+          for (int s = 0; s < C::kQKSub; ++s)
+            tma_load_3d_hint(smem + C::kKOff + st * C::kQKTileBytes + s * C::kQKSubBytes, &tm_k,
                              &bars->k_full[st], s * 64, kt * kBlockN, u.bh, keep);
           mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
 #pragma unroll
@@ -355,13 +362,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t k_base = smem_u32(smem + C::kKOff);
       auto issue_s = [&](int qb, int i, int st) {
         if (leader) {
-          const uint32_t qa = q_base + (qb * 2 + i) * C::kTileBytes;
-          const uint32_t ka = k_base + st * C::kTileBytes;
+          const uint32_t qa = q_base + (qb * 2 + i) * C::kQKTileBytes;
+          const uint32_t ka = k_base + st * C::kQKTileBytes;
+          if constexpr (QK8) {
+            // e4m3: K = 32 codes = 32 bytes per instruction inside one swizzled row
+            constexpr uint32_t kIdescS8 = idesc_e4m3(kBlockM, kBlockN);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kSubBytes + (kk & 3) * 32;
-            mma_ss(tmem + C::col_s(i), sdesc_sw128(qa + off, 16, 1024),
-                   sdesc_sw128(ka + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 32; ++kk) {
+              const uint32_t off = kk * 32;
+              const uint64_t da = (D == 128) ? sdesc_sw128(qa + off, 16, 1024) : sdesc_sw64(qa + off, 16, 512);
+              const uint64_t db = (D == 128) ? sdesc_sw128(ka + off, 16, 1024) : sdesc_sw64(ka + off, 16, 512);
+              mma_ss_f8(tmem + C::col_s(i), da, db, kIdescS8, kk > 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::kSubBytes + (kk & 3) * 32;
+              mma_ss(tmem + C::col_s(i), sdesc_sw128(qa + off, 16, 1024),
+                     sdesc_sw128(ka + off, 16, 1024), kIdescS, kk > 0 ? 1u : 0u);
+            }
           }
           mma_commit(&bars->s_full[i]);
         }

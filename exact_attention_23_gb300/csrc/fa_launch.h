@@ -23,6 +23,8 @@ struct FwdLaunch {
 // Each returns the CUDA error of the launch (cudaSuccess when enqueued).
 cudaError_t launch_fwd_d64(const FwdLaunch& a, bool causal);
 cudaError_t launch_fwd_d128(const FwdLaunch& a, bool causal);
+// Q and K as e4m3 codes (tensor maps over bytes), d ∈ {64, 128}.
+cudaError_t launch_fwd_fp8(const FwdLaunch& a, int d, bool causal);
 
 // General form (Tq ≠ Tk, bottom-right causal, block masks, key ranges): the forward kernel
 // with GEN = true, then, when a.p.n_splits > 1, the merge of the partial results.

@@ -274,6 +274,18 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// D(TMEM) (+)= A(SMEM desc) * B(SMEM desc), kind::f8f6f4 (8-bit inputs, fp32 accumulate;
+// K = 32 elements per instruction).
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 async op issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -296,6 +308,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_ab(uint32_t M, uint32_t N, boo
   return idesc_bf16(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
 }
 
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0), fp32 D,
+// both K-major, dense.
+__host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.
 //   bits 0-13 start address >> 4, 16-29 leading byte offset >> 4,
 //   32-45 stride byte offset >> 4, 46-47 = 1 (descriptor version), 61-63 = 2 (128B swizzle).
@@ -306,6 +324,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Shared-memory matrix descriptor, 64-byte swizzle (layout code 4): rows of 64 bytes whose
+// 16-byte chunks are permuted within each group of 8 rows (SBO = 8 rows = 512 bytes), the
+// layout a TMA load with 64-byte swizzle produces.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(4) << 61;
   return d;
 }
 

@@ -101,3 +101,33 @@ def make_do(B: int, H: int, T: int, d: int, seed: int):
 
 def workload_do(w: Workload):
     return make_do(w.B, w.H, w.T, w.d, w.seed)
+
+
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor FP8 (e4m3) quantisation of an input: scale = max|x| / 448, codes =
+    round-to-nearest-even of x / scale. Returns (codes as a uint8 tensor of x's shape,
+    scale as a Python float); the value a code stands for is e4m3(code) · scale."""
+    x = x.float()
+    amax = float(x.abs().max())
+    # a float32 value, so the scale handed to the C ABI is exactly the one the codes use
+    scale = torch.tensor(amax / E4M3_MAX, dtype=torch.float32).item() if amax > 0 else 1.0
+    codes = (x / scale).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+    return codes, scale
+
+
+def dequantize_e4m3(codes: torch.Tensor, scale: float):
+    """The exact values of e4m3 codes times the scale, as fp64 numpy (every e4m3 value and
+    its product with a float scale is exact in fp64)."""
+    return codes.view(torch.float8_e4m3fn).double().numpy() * scale
+
+
+def make_qk_fp8(B: int, H: int, T: int, d: int, seed: int):
+    """The workload's q and k (make_qkv with this seed) quantised to e4m3 per tensor, and its
+    v in bf16: (q8, q_scale, k8, k_scale, v)."""
+    q, k, v = make_qkv(B, H, T, d, seed)
+    q8, sq = quantize_e4m3(q)
+    k8, sk = quantize_e4m3(k)
+    return q8, sq, k8, sk, v

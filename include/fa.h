@@ -230,6 +230,22 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
                    const float* lse, void* dq, void* dk, void* dv, int B, int H, int T, int d,
                    int causal, float scale, void* stream);
 
+/*
+ * fa_fwd_fp8 — the forward with Q and K given as FP8 (e4m3) codes with per-tensor scales:
+ * the query and key values are q8·q_scale and k8·k_scale, and S = scale·Q·Kᵀ is computed
+ * from the codes on the tensor cores' 8-bit path (exact products, fp32 sums) with
+ * q_scale·k_scale folded into the softmax's exponent factor. V stays bf16 and P is rounded
+ * to bf16 as in fa_fwd, so the output carries the bf16 path's error on the quantised
+ * inputs. Low-precision modes are the direction step V3 of "内核案例研究：Flash Attention"
+ * points to ("最近在 V3 版本中").
+ *
+ *   q8, k8           : const uint8*, [B, H, T, d] e4m3 codes, device memory, 16-byte aligned
+ *   q_scale, k_scale : finite and > 0
+ *   v, o, lse, B, H, T, d, causal, scale, stream : as for fa_fwd (d ∈ {64, 128})
+ */
+int fa_fwd_fp8(const void* q8, const void* k8, const void* v, void* o, float* lse, float q_scale,
+               float k_scale, int B, int H, int T, int d, int causal, float scale, void* stream);
+
 /* Static text for a status code (never NULL). */
 const char* fa_strerror(int status);
 

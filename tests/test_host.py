@@ -259,3 +259,41 @@ def test_general_forms_without_device_report_unsupported(lib):
     assert _bs_call() == fa.FA_ERR_UNSUPPORTED_DEVICE
     assert _bs_call(mask_heads=2) == fa.FA_ERR_UNSUPPORTED_DEVICE
     assert fa.fa_fwd_kv_workspace_size(1, 1, 1, 1000, 64, 0) == 0   # automatic choice needs a device
+
+
+# ---------------------------------------------------------------- FP8 (e4m3) query/key forward
+
+def _fp8_call(q8=A, k8=A + SZ, v=A + 2 * SZ, o=A + 3 * SZ, lse=A + 4 * SZ, q_scale=0.01,
+              k_scale=0.02, B=1, H=2, T=1000, d=64, causal=1, scale=0.125):
+    return fa.fa_fwd_fp8(q8, k8, v, o, lse, q_scale, k_scale, B, H, T, d, causal, scale, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q8=0), fa.FA_ERR_INVALID_ARG),
+    (dict(k8=0), fa.FA_ERR_INVALID_ARG),
+    (dict(T=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_INVALID_ARG),
+    (dict(q_scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(k_scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(q_scale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(q8=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(o=A + SZ + 4096), fa.FA_ERR_INVALID_ARG),     # o overlaps the codes of k
+])
+def test_fwd_fp8_host_validation(lib, kw, want):
+    assert _fp8_call(**kw) == want
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="only meaningful on a machine without a CUDA device")
+def test_fwd_fp8_without_device_reports_unsupported(lib):
+    assert _fp8_call() == fa.FA_ERR_UNSUPPORTED_DEVICE
+    # o directly after q's one-byte codes does not overlap them
+    assert _fp8_call(o=A + 2 * 1000 * 64) == fa.FA_ERR_UNSUPPORTED_DEVICE
+
+
+def test_fwd_fp8_wrapper_rejects_bf16_codes():
+    import torch
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fwd_fp8(x, 1.0, x, 1.0, x)

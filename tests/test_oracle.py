@@ -240,3 +240,39 @@ def test_backward_pins_catch_forward_mistake(name, monkeypatch):
 
 def test_unmodified_oracle_passes_every_pin():
     assert pins.run_all(oa, ALL_PINS) == []
+
+
+def test_e4m3_decoding_matches_the_format():
+    """The FP8 inputs' decoder (a library cast) against the e4m3 definition: 1 sign bit,
+    4 exponent bits with bias 7, 3 mantissa bits; exponent 0 is subnormal (m/8 · 2^-6);
+    S.1111.111 is NaN and there is no infinity, so the largest value is 1.75 · 2^8 = 448."""
+    import torch
+    from exact_attention_23_gb300 import inputs
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    got = inputs.dequantize_e4m3(codes, 1.0)
+    for c in range(256):
+        sign = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 0xF, c & 0x7
+        if e == 0xF and m == 0x7:
+            assert np.isnan(got[c]), c
+            continue
+        want = sign * (m / 8.0 * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7))
+        assert got[c] == want, (c, got[c], want)
+    assert np.nanmax(got) == inputs.E4M3_MAX
+
+
+def test_e4m3_quantisation_round_trip():
+    """Quantised values are the nearest e4m3 values (relative error ≤ 2^-4) and the scale
+    maps the largest magnitude to 448."""
+    import torch
+    from exact_attention_23_gb300 import inputs
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(1000, generator=g) * 3.0
+    codes, sc = inputs.quantize_e4m3(x)
+    back = inputs.dequantize_e4m3(codes, sc)
+    xf = x.double().numpy()
+    # the scale is rounded to fp32, so the largest magnitude comes back to within 2^-23
+    assert abs(np.abs(back).max() - np.abs(xf).max()) <= 2.0 ** -23 * np.abs(xf).max()
+    assert np.float32(sc) == sc
+    big = np.abs(xf) > sc * 2.0 ** -6 * 8   # normal range of e4m3
+    assert np.all(np.abs(back[big] - xf[big]) <= 2.0 ** -4 * np.abs(xf[big]) + 1e-12)

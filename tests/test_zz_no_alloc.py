@@ -17,7 +17,7 @@ def test_noalloc_rejects_sizes_beyond_the_reservation():
     assert fa.fa_bwd_workspace_size(1, 12, 10496, 64) <= _binding.FA_BWD_NOALLOC_SCRATCH_BYTES
     ptrs = [A + i * (1 << 32) for i in range(9)]
     assert _binding.fa_bwd_noalloc(*ptrs, 1, 12, 10497, 64, 1, 0.125, None) == fa.FA_ERR_INVALID_ARG
-    assert _binding.fa_bwd_noalloc(*ptrs, 1, 12, 128, 128, 1, 0.125, None) == fa.FA_ERR_INVALID_ARG
+    assert _binding.fa_bwd_noalloc(*ptrs, 1, 12, 128, 96, 1, 0.125, None) == fa.FA_ERR_INVALID_ARG
     assert _binding.fa_bwd_noalloc(0, *ptrs[1:], 1, 12, 128, 64, 1, 0.125, None) == fa.FA_ERR_INVALID_ARG
 
 
