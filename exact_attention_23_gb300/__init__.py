@@ -32,6 +32,8 @@ from ._binding import (  # noqa: F401
     fa_fwd_block_sparse,
     fa_fwd_ex,
     fa_fwd_fp8,
+    fa_fwd_host,
+    fa_fwd_host_workspace_size,
     fa_fwd_kv,
     fa_fwd_kv_workspace_size,
     lib,
@@ -82,6 +84,45 @@ def fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=
                        stream)
     if rc != FA_OK:
         raise FAError(rc, "fa_fwd")
+    return out, lse
+
+
+def fwd_host(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=None,
+             heads_per_chunk: int = 0, workspace=None, device=None, synchronize: bool = True):
+    """Forward over host tensors (CPU bf16 [B, H, T, d], contiguous; page-locked for
+    overlapped copies) through fa_fwd_host on ``device``'s current stream. Outputs are host
+    tensors (page-locked when not given). With ``synchronize`` the stream is synchronised
+    before returning; otherwise the caller must do so before reading them."""
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.bfloat16 \
+                or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous host bf16 [B, H, T, d] tensor")
+    if q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k and v must have the same shape")
+    B, H, T, d = q.shape
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
+        else torch.device(device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((B, H, T), dtype=torch.float32, pin_memory=True)
+    with torch.cuda.device(dev):
+        if workspace is None:
+            need = fa_fwd_host_workspace_size(B, H, T, d, heads_per_chunk)
+            if need == 0:
+                raise FAError(FA_ERR_INVALID_ARG, "fa_fwd_host_workspace_size")
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        s = torch.cuda.current_stream(dev)
+        rc = fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         lse.data_ptr(), B, H, T, d, causal, scale, heads_per_chunk,
+                         workspace.data_ptr(), workspace.numel(), s.cuda_stream)
+        if rc != FA_OK:
+            raise FAError(rc, "fa_fwd_host")
+        if synchronize:
+            s.synchronize()
     return out, lse
 
 

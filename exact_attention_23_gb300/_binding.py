@@ -24,7 +24,7 @@ FA_FLAG_TEST_STARVE_Q = 1
 FA_BWD_NOALLOC_SCRATCH_BYTES = 33554432
 
 # Every symbol include/fa.h declares.
-EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_fwd_fp8", "fa_fwd_kv_workspace_size", "fa_fwd_kv",
+EXPORTS = ("fa_fwd", "fa_fwd_ex", "fa_fwd_fp8", "fa_fwd_host_workspace_size", "fa_fwd_host", "fa_fwd_kv_workspace_size", "fa_fwd_kv",
            "fa_fwd_block_sparse", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_ex",
            "fa_bwd_noalloc", "fa_strerror", "fa_version")
 
@@ -55,6 +55,10 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_ex.restype = i
             sz = ctypes.c_size_t
             L.fa_fwd_fp8.argtypes = [vp] * 5 + [f, f, i, i, i, i, i, f, vp]
+            L.fa_fwd_host_workspace_size.argtypes = [i, i, i, i, i]
+            L.fa_fwd_host_workspace_size.restype = sz
+            L.fa_fwd_host.argtypes = [vp] * 5 + [i, i, i, i, i, f, i, vp, sz, vp]
+            L.fa_fwd_host.restype = i
             L.fa_fwd_fp8.restype = i
             L.fa_fwd_kv_workspace_size.argtypes = [i, i, i, i, i, i]
             L.fa_fwd_kv_workspace_size.restype = sz
@@ -139,3 +143,13 @@ def fa_fwd_block_sparse(q, k, v, o, lse, block_mask, mask_heads, B, H, T, d, cau
 def fa_fwd_fp8(q8, k8, v, o, lse, q_scale, k_scale, B, H, T, d, causal, scale, stream) -> int:
     return lib().fa_fwd_fp8(q8, k8, v, o, lse, float(q_scale), float(k_scale), B, H, T, d,
                             int(bool(causal)), float(scale), stream)
+
+
+def fa_fwd_host_workspace_size(B, H, T, d, heads_per_chunk=0) -> int:
+    return int(lib().fa_fwd_host_workspace_size(B, H, T, d, heads_per_chunk))
+
+
+def fa_fwd_host(q, k, v, o, lse, B, H, T, d, causal, scale, heads_per_chunk, ws, ws_bytes,
+                stream) -> int:
+    return lib().fa_fwd_host(q, k, v, o, lse, B, H, T, d, int(bool(causal)), float(scale),
+                             heads_per_chunk, ws, ws_bytes, stream)

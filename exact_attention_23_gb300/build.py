@@ -23,7 +23,7 @@ LIB = os.path.join(PKG, "libfa.so")
 SOURCES = ["fa_api.cu", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_fwd_fp8.cu", "fa_fwd_gen_d64.cu",
            "fa_fwd_gen_d128.cu", "fa_fwd_ext_api.cu", "fa_decode.cu", "fa_bwd_d64.cu", "fa_bwd_d128.cu",
            "fa_bwd_api.cu",
-           "fa_noalloc.cu"]
+           "fa_noalloc.cu", "fa_hostio.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I", INCLUDE, "-I", CSRC]

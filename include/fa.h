@@ -246,6 +246,34 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
 int fa_fwd_fp8(const void* q8, const void* k8, const void* v, void* o, float* lse, float q_scale,
                float k_scale, int B, int H, int T, int d, int causal, float scale, void* stream);
 
+/*
+ * fa_fwd_host — the forward of fa_fwd on tensors that live in HOST memory. The B·H heads are
+ * taken in chunks of `heads_per_chunk` (0: the library picks enough heads to give every SM
+ * two work units); each chunk is copied into a device staging buffer, attended with fa_fwd's
+ * kernel and copied back. Copies in, computation and copies out run on three streams with
+ * three staging buffers, so a chunk's transfers overlap its neighbours' computation. The
+ * kernels run on `stream`; the copies on two streams the library creates once per device.
+ * Everything is enqueued behind the work already on `stream`, and `stream` is made to wait
+ * for the last copy out: o and lse may be read once `stream` has been synchronised, and the
+ * workspace may then be reused. Results are bit-identical to fa_fwd on the same values.
+ *
+ *   q, k, v   : const bf16*, [B, H, T, d] contiguous, host memory (page-locked memory lets
+ *               the copies run asynchronously; pageable memory works, without the overlap)
+ *   o, lse    : bf16* [B, H, T, d] and float* [B, H, T], host memory, written asynchronously
+ *   workspace : device memory of at least fa_fwd_host_workspace_size(B, H, T, d,
+ *               heads_per_chunk) bytes, 256-byte aligned, owned by the caller
+ *   B, H, T, d, causal, scale : as for fa_fwd
+ *
+ * Errors: the argument checks of fa_fwd (applied to the host tensors), plus a null,
+ * misaligned or too small workspace and heads_per_chunk < 0, are returned before anything
+ * is enqueued. A CUDA error while enqueuing returns FA_ERR_LAUNCH; chunks enqueued before it
+ * still run.
+ */
+size_t fa_fwd_host_workspace_size(int B, int H, int T, int d, int heads_per_chunk);
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int T, int d, int causal, float scale, int heads_per_chunk, void* workspace,
+                size_t workspace_bytes, void* stream);
+
 /* Static text for a status code (never NULL). */
 const char* fa_strerror(int status);
 

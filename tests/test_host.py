@@ -297,3 +297,52 @@ def test_fwd_fp8_wrapper_rejects_bf16_codes():
     x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fwd_fp8(x, 1.0, x, 1.0, x)
+
+
+# ---------------------------------------------------------------- host-memory forward
+
+def _host_call(q=A, k=A + SZ, v=A + 2 * SZ, o=A + 3 * SZ, lse=A + 4 * SZ, B=1, H=4, T=1000,
+               d=64, causal=1, scale=0.125, hpc=2, ws=A + 5 * SZ, ws_bytes=1 << 30):
+    return fa.fa_fwd_host(q, k, v, o, lse, B, H, T, d, causal, scale, hpc, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=0), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=0), fa.FA_ERR_INVALID_ARG),
+    (dict(T=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_INVALID_ARG),
+    (dict(hpc=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=A + 5 * SZ + 128), fa.FA_ERR_MISALIGNED),
+    (dict(o=A + 4096), fa.FA_ERR_INVALID_ARG),            # o overlaps q
+    (dict(ws_bytes=1024), fa.FA_ERR_INVALID_ARG),          # workspace too small
+])
+def test_fwd_host_validation(lib, kw, want):
+    assert _host_call(**kw) == want
+
+
+def test_fwd_host_workspace_size(lib):
+    # three staging buffers of c heads: q, k, v, o (bf16) and lse (fp32), each 256-aligned
+    def chunk(c, T, d):
+        r = lambda x: -(-x // 256) * 256
+        return 4 * r(c * T * d * 2) + r(c * T * 4)
+    assert fa.fa_fwd_host_workspace_size(2, 6, 1000, 64, 4) == 3 * chunk(4, 1000, 64)
+    assert fa.fa_fwd_host_workspace_size(2, 6, 1000, 128, 100) == 3 * chunk(12, 1000, 128)
+    assert fa.fa_fwd_host_workspace_size(2, 6, 1000, 96, 4) == 0
+    assert fa.fa_fwd_host_workspace_size(2, 6, 1000, 64, -1) == 0
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="only meaningful on a machine without a CUDA device")
+def test_fwd_host_without_device_reports_unsupported(lib):
+    assert _host_call() == fa.FA_ERR_UNSUPPORTED_DEVICE
+    assert _host_call(hpc=0) == fa.FA_ERR_UNSUPPORTED_DEVICE    # automatic chunking
+    assert fa.fa_fwd_host_workspace_size(1, 4, 1000, 64, 0) == 0
+
+
+def test_fwd_host_wrapper_rejects_device_or_wrong_dtype():
+    import torch
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.float32)
+    with pytest.raises(ValueError):
+        fa.fwd_host(x, x, x)
