@@ -584,46 +584,72 @@ __global__ void __launch_bounds__(kThreads, 1)
           masked = (CAUSAL && kt == qt) || (k0 + kBlockN > p.T);
         }
 
-        // S in two halves: the second half loads while the first is masked and maxed.
+        // S into registers. D = 64: all four 32-column loads in flight before one wait (one
+        // TMEM round trip). D = 128: in two halves, the second loading while the first is
+        // masked and maxed (measured faster there).
         uint32_t s[kBlockN];
-        tmem_ld32(t_s + 0, s);
-        tmem_ld32(t_s + 32, s + 32);
-        tmem_ld_wait();
-        reg_fence32(s);
-        reg_fence32(s + 32);
-        tmem_ld32(t_s + 64, s + 64);
-        tmem_ld32(t_s + 96, s + 96);
-        if (masked) {
-#pragma unroll
-          for (int t = 0; t < 64; ++t)
-            if (t >= lim) s[t] = __float_as_uint(-INFINITY);
-        }
         float mx[8];
+        if constexpr (D == 64) {
+          tmem_ld32(t_s + 0, s);
+          tmem_ld32(t_s + 32, s + 32);
+          tmem_ld32(t_s + 64, s + 64);
+          tmem_ld32(t_s + 96, s + 96);
+          tmem_ld_wait();
+          reg_fence32(s);
+          reg_fence32(s + 32);
+          reg_fence32(s + 64);
+          reg_fence32(s + 96);
+          if constexpr (C::kSepP) {
+            // S_i is in registers: the tensor core may overwrite it with the next S_i.
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->s_free[wg]);
+          }
+          FA_TRACE(20 + wg, j);
+          if (masked) {
 #pragma unroll
-        for (int a = 0; a < 8; ++a) mx[a] = fmaxf(u2f(s[2 * a]), u2f(s[2 * a + 1]));
+            for (int t = 0; t < kBlockN; ++t)
+              if (t >= lim) s[t] = __float_as_uint(-INFINITY);
+          }
 #pragma unroll
-        for (int t = 16; t < 64; t += 16)
+          for (int a = 0; a < 8; ++a) mx[a] = fmaxf(u2f(s[2 * a]), u2f(s[2 * a + 1]));
 #pragma unroll
-          for (int a = 0; a < 8; ++a) mx[a] = fmax3(mx[a], u2f(s[t + 2 * a]), u2f(s[t + 2 * a + 1]));
-        tmem_ld_wait();
-        reg_fence32(s + 64);
-        reg_fence32(s + 96);
-        if constexpr (C::kSepP) {
-          // S_i is in registers: the tensor core may overwrite it with the next S_i.
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->s_free[wg]);
+          for (int t = 16; t < kBlockN; t += 16)
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mx[a] = fmax3(mx[a], u2f(s[t + 2 * a]), u2f(s[t + 2 * a + 1]));
+        } else {
+          tmem_ld32(t_s + 0, s);
+          tmem_ld32(t_s + 32, s + 32);
+          tmem_ld_wait();
+          reg_fence32(s);
+          reg_fence32(s + 32);
+          tmem_ld32(t_s + 64, s + 64);
+          tmem_ld32(t_s + 96, s + 96);
+          if (masked) {
+#pragma unroll
+            for (int t = 0; t < 64; ++t)
+              if (t >= lim) s[t] = __float_as_uint(-INFINITY);
+          }
+#pragma unroll
+          for (int a = 0; a < 8; ++a) mx[a] = fmaxf(u2f(s[2 * a]), u2f(s[2 * a + 1]));
+#pragma unroll
+          for (int t = 16; t < 64; t += 16)
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mx[a] = fmax3(mx[a], u2f(s[t + 2 * a]), u2f(s[t + 2 * a + 1]));
+          tmem_ld_wait();
+          reg_fence32(s + 64);
+          reg_fence32(s + 96);
+          FA_TRACE(20 + wg, j);
+          if (masked) {
+#pragma unroll
+            for (int t = 64; t < kBlockN; ++t)
+              if (t >= lim) s[t] = __float_as_uint(-INFINITY);
+          }
+#pragma unroll
+          for (int t = 64; t < kBlockN; t += 16)
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mx[a] = fmax3(mx[a], u2f(s[t + 2 * a]), u2f(s[t + 2 * a + 1]));
         }
-        FA_TRACE(20 + wg, j);
-        if (masked) {
-#pragma unroll
-          for (int t = 64; t < kBlockN; ++t)
-            if (t >= lim) s[t] = __float_as_uint(-INFINITY);
-        }
-#pragma unroll
-        for (int t = 64; t < kBlockN; t += 16)
-#pragma unroll
-          for (int a = 0; a < 8; ++a) mx[a] = fmax3(mx[a], u2f(s[t + 2 * a]), u2f(s[t + 2 * a + 1]));
         const float m_tile =
             fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c;
         FA_TRACE(40 + wg, j);
