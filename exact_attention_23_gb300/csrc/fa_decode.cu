@@ -7,17 +7,19 @@ namespace fa {
 cudaError_t launch_decode(const DecodeParams& p, int d, unsigned combine_grid,
                           cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.n_splits);
-  if (d == 64) fa_decode_kernel<64><<<grid, kDecThreads, 0, stream>>>(p);
-  else fa_decode_kernel<128><<<grid, kDecThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = (d == 64) ? launch_pdl(fa_decode_kernel<64>, grid, kDecThreads, stream, p)
+                            : launch_pdl(fa_decode_kernel<128>, grid, kDecThreads, stream, p);
   if (e != cudaSuccess || p.n_splits <= 1) return e;
-  if (d == 64)
-    fa_fwd_combine_kernel<64><<<combine_grid, 256, 0, stream>>>(p.o_part, p.lse_part, p.o, p.lse,
-                                                                p.n_splits, p.BH);
-  else
-    fa_fwd_combine_kernel<128><<<combine_grid, 256, 0, stream>>>(p.o_part, p.lse_part, p.o, p.lse,
-                                                                 p.n_splits, p.BH);
-  return cudaGetLastError();
+  // one merge thread per (row, 8 columns)
+  const unsigned long long items = static_cast<unsigned long long>(p.BH) * (d / 8);
+  const unsigned need = static_cast<unsigned>((items + 255) / 256);
+  const unsigned cg = need < combine_grid ? need : combine_grid;
+  const float* op = p.o_part;
+  const float* lp = p.lse_part;
+  return (d == 64) ? launch_pdl(fa_fwd_combine_kernel<64>, cg, 256, stream, op, lp, p.o, p.lse,
+                                p.n_splits, p.BH)
+                   : launch_pdl(fa_fwd_combine_kernel<128>, cg, 256, stream, op, lp, p.o, p.lse,
+                                p.n_splits, p.BH);
 }
 
 }  // namespace fa

@@ -56,6 +56,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecCtasPerSm)
   constexpr int kWarps = kDecThreads / 32;
   __shared__ float wm[kWarps], wl[kWarps];
   __shared__ __align__(16) float wo[kWarps][D];
+  // Launched as a programmatic dependent: the previous kernel on the stream (possibly the
+  // last merge, which reads o_part) must be complete before anything is read or written.
+  pdl_wait();
+  pdl_launch_dependents();
   const int bh = blockIdx.x % p.BH;
   const int split = blockIdx.x / p.BH;
   const int kb = split * p.keys_per_split;

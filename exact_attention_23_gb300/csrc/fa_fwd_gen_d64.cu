@@ -22,9 +22,10 @@ static cudaError_t launch_gen(const FwdLaunch& a, unsigned combine_grid) {
   fn<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.p.n_splits <= 1) return e;
-  fa_fwd_combine_kernel<D><<<combine_grid, 256, 0, a.stream>>>(
-      a.p.o_part, a.p.lse_part, a.p.o, a.p.lse, a.p.n_splits, a.p.BH * a.p.T);
-  return cudaGetLastError();
+  const float* op = a.p.o_part;
+  const float* lp = a.p.lse_part;
+  return launch_pdl(fa_fwd_combine_kernel<D>, combine_grid, 256, a.stream, op, lp, a.p.o,
+                    a.p.lse, a.p.n_splits, a.p.BH * a.p.T);
 }
 
 cudaError_t launch_fwd_gen_d64(const FwdLaunch& a, bool causal, unsigned combine_grid) {

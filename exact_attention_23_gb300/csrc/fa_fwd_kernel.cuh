@@ -771,6 +771,9 @@ __global__ void __launch_bounds__(256) fa_fwd_combine_kernel(const float* __rest
                                                              float* __restrict__ lse,
                                                              int n_splits, int rows) {
   constexpr int L = D / 8;
+  // Launched as a programmatic dependent of the kernel that wrote the partials.
+  pdl_wait();
+  pdl_launch_dependents();
   const size_t total = static_cast<size_t>(rows) * L;
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;

@@ -13,6 +13,25 @@ namespace fa {
 
 constexpr int kMaxDevices = 64;
 
+// Launches kernel<<<grid, block, 0, stream>>>(args...) as a programmatic dependent of the
+// previous kernel on the stream (its launch overlaps that kernel's tail; the kernel itself
+// waits for it with pdl_wait()).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 struct FwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v;
   FwdParams p;

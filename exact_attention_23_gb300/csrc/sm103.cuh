@@ -45,6 +45,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization
+// may start before the previous kernel on its stream has finished; pdl_wait() blocks until
+// that kernel has completed and its memory is visible (a no-op without such a launch), and
+// pdl_launch_dependents() lets the next such kernel be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
