@@ -19,16 +19,16 @@ static cudaError_t launch_bwd(const BwdLaunch& a) {
     if (e != cudaSuccess) return e;
     done[dev / 64].fetch_or(bit, std::memory_order_acq_rel);
   }
-  fa_bwd_prep_kernel<D><<<a.grid_prep, 256, 0, a.stream>>>(a.o, a.dout, a.lse, a.lse2, a.dvec,
-                                                           a.p.dq_acc, a.p.T, a.p.T_pad, a.p.BH);
-  cudaError_t e = cudaGetLastError();
+  // All three as programmatic dependents: each one's launch and set-up overlap the tail of
+  // the kernel before it, and each waits for it (pdl_wait) before reading its results.
+  cudaError_t e = launch_pdl(fa_bwd_prep_kernel<D>, a.grid_prep, 256, 0, a.stream, a.o, a.dout,
+                             a.lse, a.lse2, a.dvec, a.p.dq_acc, a.p.T, a.p.T_pad, a.p.BH);
   if (e != cudaSuccess) return e;
-  fn<<<a.grid_main, kBwdThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.p);
-  e = cudaGetLastError();
+  e = launch_pdl(fn, a.grid_main, kBwdThreads, smem, a.stream, a.tm_q, a.tm_k, a.tm_v, a.tm_do,
+                 a.p);
   if (e != cudaSuccess) return e;
-  fa_bwd_dq_kernel<D><<<a.grid_dq, 256, 0, a.stream>>>(a.p.dq_acc, a.dq, a.p.T, a.p.n_qt, a.p.BH,
-                                                       a.p.scale);
-  return cudaGetLastError();
+  return launch_pdl(fa_bwd_dq_kernel<D>, a.grid_dq, 256, 0, a.stream, a.p.dq_acc, a.dq, a.p.T,
+                    a.p.n_qt, a.p.BH, a.p.scale);
 }
 
 cudaError_t launch_bwd_d128(const BwdLaunch& a, bool causal) {

@@ -19,12 +19,11 @@ static cudaError_t launch_gen(const FwdLaunch& a, unsigned combine_grid) {
     if (e != cudaSuccess) return e;
     done[dev / 64].fetch_or(bit, std::memory_order_acq_rel);
   }
-  fn<<<a.grid, kThreads, smem, a.stream>>>(a.tm_q, a.tm_k, a.tm_v, a.p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(fn, a.grid, kThreads, smem, a.stream, a.tm_q, a.tm_k, a.tm_v, a.p);
   if (e != cudaSuccess || a.p.n_splits <= 1) return e;
   const float* op = a.p.o_part;
   const float* lp = a.p.lse_part;
-  return launch_pdl(fa_fwd_combine_kernel<D>, combine_grid, 256, a.stream, op, lp, a.p.o,
+  return launch_pdl(fa_fwd_combine_kernel<D>, combine_grid, 256, 0, a.stream, op, lp, a.p.o,
                     a.p.lse, a.p.n_splits, a.p.BH * a.p.T);
 }
 

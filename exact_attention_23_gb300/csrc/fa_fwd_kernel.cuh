@@ -276,6 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  // Launched as a programmatic dependent: the set-up above overlapped the previous kernel's
+  // tail; nothing in global memory is touched before that kernel has completed.
+  pdl_wait();
+  pdl_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort, p.status, p.timeout_ns};
   const WaitCtl drain{&bars->never, nullptr, p.timeout_ns};

@@ -13,16 +13,16 @@ namespace fa {
 
 constexpr int kMaxDevices = 64;
 
-// Launches kernel<<<grid, block, 0, stream>>>(args...) as a programmatic dependent of the
-// previous kernel on the stream (its launch overlaps that kernel's tail; the kernel itself
-// waits for it with pdl_wait()).
+// Launches kernel<<<grid, block, smem, stream>>>(args...) as a programmatic dependent of
+// the previous kernel on the stream: its launch and set-up overlap that kernel's tail, and
+// the kernel waits for it with pdl_wait() before touching global memory.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block,
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
                        cudaStream_t stream, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
