@@ -54,6 +54,7 @@ bool sizes_ok(int B, int H, int T, int d) {
   if (B <= 0 || H <= 0 || T <= 0 || (d != 64 && d != 128)) return false;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > INT32_MAX) return false;
+  if (static_cast<long long>(T) * d * 2 >= (1LL << 40)) return false;  // fa_fwd's TMA stride limit
   return BH * T * d < (1LL << 61) / 2;
 }
 
