@@ -24,7 +24,7 @@ static cudaError_t launch_bwd(const BwdLaunch& a) {
   cudaError_t e = launch_pdl(fa_bwd_prep_kernel<D>, a.grid_prep, 256, 0, a.stream, a.o, a.dout,
                              a.lse, a.lse2, a.dvec, a.p.dq_acc, a.p.T, a.p.T_pad, a.p.BH);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(fn, a.grid_main, kBwdThreads, smem, a.stream, a.tm_q, a.tm_k, a.tm_v, a.tm_do,
+  e = launch_pdl(fn, a.grid_main, BwdCfg<D>::kThreads, smem, a.stream, a.tm_q, a.tm_k, a.tm_v, a.tm_do,
                  a.p);
   if (e != cudaSuccess) return e;
   return launch_pdl(fa_bwd_dq_kernel<D>, a.grid_dq, 256, 0, a.stream, a.p.dq_acc, a.dq, a.p.T,
