@@ -64,7 +64,7 @@ struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kBQ = (D == 64) ? 128 : 64;    // query rows per tile
   // Compute warpgroups, each owning kNC query columns of a tile (32 at either head dim).
-  static constexpr int kCWG = (D == 64) ? 4 : 2;
+  static constexpr int kCWG = (D == 64) ? 4 : 2;  // (4 at d = 128, 16 columns each: 3 % slower)
   static constexpr int kNC = kBQ / kCWG;
   static constexpr int kComputeWarps = 4 * kCWG;
   // Warp roles after the compute warps: 4 dQ drain warps, score issuer, gradient issuer,
@@ -146,6 +146,23 @@ constexpr uint32_t kBwdFlagStarveQ = 1u;  // FA_FLAG_TEST_STARVE_Q
 //   dq_acc_offset(bh, i, n_qt, c4, r, d) is query row r, columns 4·c4 .. 4·c4+3.
 // d = 128 (dQᵀ: thread = head dim c of a 64-query tile): [bh][tile][16][128 dims][4 rows];
 //   dq_acc_offset_t(bh, i, n_qt, g, c) is head dim c of query rows 4·g .. 4·g+3.
+// N consecutive TMEM columns (N = 16 or a multiple of 32) of the warp's 32 lanes into r,
+// with one wait for all of them.
+template <int N>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
+  if constexpr (N == 16) {
+    tmem_ld16(taddr, r);
+    tmem_ld_wait();
+    reg_fence16(r);
+  } else {
+#pragma unroll
+    for (int h = 0; h < N / 32; ++h) tmem_ld32(taddr + h * 32, r + h * 32);
+    tmem_ld_wait();
+#pragma unroll
+    for (int h = 0; h < N / 32; ++h) reg_fence32(r + h * 32);
+  }
+}
+
 __host__ __device__ __forceinline__ size_t dq_acc_offset(int bh, int i, int n_qt, int c4, int r,
                                                          int d) {
   return ((((size_t)bh * n_qt + i) * (size_t)(d / 4) + c4) * 128u + r) * 4u;
@@ -572,11 +589,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       FA_TRACE(10, t);
       tc_fence_after_sync();
       uint32_t s[NC];
-#pragma unroll
-      for (int h = 0; h < NC / 32; ++h) tmem_ld32(tmem + lane_off + C::kColS + g * NC + h * 32, s + h * 32);
-      tmem_ld_wait();
-#pragma unroll
-      for (int h = 0; h < NC / 32; ++h) reg_fence32(s + h * 32);
+      tmem_load_cols<NC>(tmem + lane_off + C::kColS + g * NC, s);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->s_free);
@@ -605,7 +618,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       for (int c = 0; c < NC / 2; ++c) pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
       tc_fence_after_sync();
       if constexpr (NC == 64) tmem_st32(tmem + lane_off + C::kColP + g * 32, pk);
-      else tmem_st16(tmem + lane_off + C::kColP + g * 16, pk);
+      else if constexpr (NC == 32) tmem_st16(tmem + lane_off + C::kColP + g * 16, pk);
+      else tmem_st8(tmem + lane_off + C::kColP + g * 8, pk);
       tmem_st_wait();
       tc_fence_before_sync();
       __syncwarp();
@@ -619,22 +633,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (t >= 2 && !(ok = mbar_wait_warp_inl(&bars->ds_free[b], ((t >> 1) - 1) & 1, wc))) break;
       FA_TRACE(15, t);
       tc_fence_after_sync();
+      // dPᵀ for this warpgroup's columns (NC = 64: in two halves, to stay within the
+      // registers of 15 warps)
+      constexpr int kDPB = (NC > 32) ? 32 : NC;  // columns per dPᵀ block
 #pragma unroll
-      for (int h = 0; h < NC / 32; ++h) {
-        uint32_t dp[32];
-        tmem_ld32(tmem + lane_off + C::kColDP + g * NC + h * 32, dp);
-        tmem_ld_wait();
-        reg_fence32(dp);
-        if (h == NC / 32 - 1) {
+      for (int h = 0; h < NC / kDPB; ++h) {
+        uint32_t dp[kDPB];
+        tmem_load_cols<kDPB>(tmem + lane_off + C::kColDP + g * NC + h * kDPB, dp);
+        if (h == NC / kDPB - 1) {
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->dp_free);
         }
-        const float4* d4 = reinterpret_cast<const float4*>(vec + C::kBQ + g * NC + h * 32);
+        const float4* d4 = reinterpret_cast<const float4*>(vec + C::kBQ + g * NC + h * kDPB);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < kDPB / 8; ++q4) {
           const float4 da = d4[2 * q4], db = d4[2 * q4 + 1];
-          const int c = h * 32 + q4 * 8;
+          const int c = h * kDPB + q4 * 8;
           const uint32_t* dq8 = dp + q4 * 8;
           float ds[8];
           ds[0] = pr[c] * (__uint_as_float(dq8[0]) - da.x);
@@ -645,7 +660,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           ds[5] = pr[c + 5] * (__uint_as_float(dq8[5]) - db.y);
           ds[6] = pr[c + 6] * (__uint_as_float(dq8[6]) - db.z);
           ds[7] = pr[c + 7] * (__uint_as_float(dq8[7]) - db.w);
-          st_row_chunk_sw128(ds_box, r, ds_chunk0 + h * 4 + q4, ds);
+          st_row_chunk_sw128(ds_box, r, ds_chunk0 + c / 8, ds);
         }
       }
       fence_proxy_async_smem();
