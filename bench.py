@@ -129,6 +129,17 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "fwd": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_api.cu"),
     "bwd": ("sm103.cuh", "fa_bwd_kernel.cuh", "fa_bwd_d64.cu", "fa_bwd_api.cu"),
+    "decode": ("sm103.cuh", "fa_decode_kernel.cuh", "fa_decode.cu", "fa_fwd_ext_api.cu"),
+    "block_sparse": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd_gen_d64.cu", "fa_fwd_ext_api.cu"),
+    "fp8": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd_fp8.cu", "fa_api.cu"),
+}
+# The committed ncu record of each pass's dominant kernel (profiles/).
+TRAFFIC_RECORDS = {
+    "fwd": "dram_traffic_fa_fwd_d64_causal_t16384.json",
+    "bwd": "dram_traffic_fa_bwd_d64_causal_t16384.json",
+    "decode": "dram_traffic_fa_decode_d64_b4h12_tk16384.json",
+    "block_sparse": "dram_traffic_fa_fwd_block_sparse_d64_t8192.json",
+    "fp8": "dram_traffic_fa_fwd_fp8_d128_causal_t16384.json",
 }
 
 
@@ -145,7 +156,7 @@ def kernel_source_sha256(which: str = "fwd") -> str:
 def _measured_traffic(which: str = "fwd"):
     """DRAM bytes per launch of the dominant kernel from the committed ncu record, or None
     when the kernel sources changed after the counters were taken."""
-    path = os.path.join(ROOT, "profiles", f"dram_traffic_fa_{which}_d64_causal_t16384.json")
+    path = os.path.join(ROOT, "profiles", TRAFFIC_RECORDS[which])
     try:
         with open(path) as f:
             rec = json.load(f)
@@ -375,7 +386,8 @@ def _fwd_fp8(args, fa, inputs, torch, dev, stream, bf16_sus, ws):
             "value": tf8, "unit": "TFLOP/s", "ms_per_call": ms8, "steps": steps,
             "bf16_same_values": {"value": tf16, "unit": "TFLOP/s", "ms_per_call": ms16},
             "roofline": {"bound": "tensor", "achieved": tf8 / ws, "peak": peak,
-                         "unit": "TFLOP/s", "frac": tf8 / ws / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": tf8 / ws / peak,
+                         "traffic": _measured_traffic("fp8"),
                          "peak_basis": "4/3 x sustained bf16 of measured (Q·Kᵀ at the "
                                        "nominal 2x 8-bit rate, P·V at bf16)"},
             "gpu_launches": 2 * steps}
@@ -409,10 +421,11 @@ def _general_forms(args, fa, inputs, torch, dev, stream, bf16_sus, hbm_peak, ws)
         "metric": "decode GB/s (bf16, B4 H12 d64, 1 query vs 16384 cached keys, causal)",
         "value": gbs, "unit": "GB/s", "us_per_call": ms * 1e3, "steps": args.steps,
         "roofline": {"bound": "hbm", "achieved": gbs / ws, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": gbs / ws / hbm_peak, "traffic": None,
+                     "frac": gbs / ws / hbm_peak, "traffic": _measured_traffic("decode"),
                      "algorithmic_bytes": byts,
-                     "kernel": "fa_fwd_kernel<64,causal,general> over split key ranges + "
-                               "fa_fwd_combine_kernel; achieved over the whole fa_fwd_kv call"},
+                     "kernel": "fa_decode_kernel<64> (CUDA cores) over split key ranges + "
+                               "fa_fwd_combine_kernel; achieved over the whole fa_fwd_kv call; "
+                               "traffic of the decode kernel"},
         "gpu_launches": 2 * args.steps,
     }
     del q, k, v, qd, o, lse, wsb
@@ -441,7 +454,7 @@ def _general_forms(args, fa, inputs, torch, dev, stream, bf16_sus, hbm_peak, ws)
         "value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "kept_blocks": kept,
         "blocks": nb * nb, "steps": args.steps,
         "roofline": {"bound": "tensor", "achieved": tf / ws, "peak": bf16_sus, "unit": "TFLOP/s",
-                     "frac": tf / ws / bf16_sus, "traffic": None,
+                     "frac": tf / ws / bf16_sus, "traffic": _measured_traffic("block_sparse"),
                      "kernel": "fa_fwd_kernel<64,non-causal,general> with a block mask; FLOPs "
                                "= 4·B·H·128²·d per kept block"},
         "gpu_launches": args.steps,
