@@ -191,8 +191,11 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
     }
   }
   // `stream` waits for the last copy out (the copy-out stream runs in order), so that
-  // synchronising it makes o and lse readable and a later call may reuse the workspace.
+  // synchronising it makes o and lse readable and a later call may reuse the workspace;
+  // and for every copy in (after an error a chunk may have been copied in but not attended).
   if (last >= 0) cudaStreamWaitEvent(st, ev_out[last % kSlots], 0);
+  if (ev_start && cudaEventRecord(ev_start, cs.in) == cudaSuccess)
+    cudaStreamWaitEvent(st, ev_start, 0);
   for (cudaEvent_t* e : all)
     if (*e) cudaEventDestroy(*e);  // released once pending work completes
   return rc;

@@ -30,6 +30,11 @@
  *   - The call is asynchronous on `stream` (a cudaStream_t; NULL means the legacy
  *     default stream). It returns after the launch is enqueued; errors that happen
  *     while the kernel runs surface at the caller's next synchronisation.
+ *   - Kernels are launched as programmatic dependents of the kernel before them on the
+ *     stream (cudaLaunchKernelEx with programmatic stream serialisation): their set-up
+ *     overlaps that kernel's tail, and they read and write global memory only after it
+ *     has completed, so stream order is kept. Earlier work of any other kind (copies,
+ *     event waits) is waited for as usual.
  *   - Argument errors are detected on the host and returned before anything is
  *     launched; nothing is written to o or lse in that case.
  *   - Thread safety: calls from several host threads are safe.
