@@ -1,14 +1,43 @@
 // Instantiations of the decode kernel (one query row per head, CUDA cores) and its launch,
 // followed by the merge of key-range partial results when the keys are split.
+#include <atomic>
+
 #include "fa_launch.h"
 
 namespace fa {
 
+namespace {
+
+// The ring's shared-memory opt-in and a full shared-memory carveout (three 66 KB CTAs per
+// SM) are per-device attributes: set once per device.
+template <int D>
+cudaError_t prepare_decode() {
+  static std::atomic<uint64_t> done[kMaxDevices / 64 + 1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const uint64_t bit = 1ull << (dev % 64);
+  if (done[dev / 64].load(std::memory_order_acquire) & bit) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(fa_decode_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       dec_smem_bytes<D>());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fa_decode_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           100);
+  if (e != cudaSuccess) return e;
+  done[dev / 64].fetch_or(bit, std::memory_order_acq_rel);
+  return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t launch_decode(const DecodeParams& p, int d, unsigned combine_grid,
                           cudaStream_t stream) {
   const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.n_splits);
-  cudaError_t e = (d == 64) ? launch_pdl(fa_decode_kernel<64>, grid, kDecThreads, 0, stream, p)
-                            : launch_pdl(fa_decode_kernel<128>, grid, kDecThreads, 0, stream, p);
+  cudaError_t e = (d == 64) ? prepare_decode<64>() : prepare_decode<128>();
+  if (e != cudaSuccess) return e;
+  e = (d == 64) ? launch_pdl(fa_decode_kernel<64>, grid, kDecBlock, dec_smem_bytes<64>(), stream, p)
+                : launch_pdl(fa_decode_kernel<128>, grid, kDecBlock, dec_smem_bytes<128>(), stream,
+                             p);
   if (e != cudaSuccess || p.n_splits <= 1) return e;
   // one merge thread per (row, 8 columns)
   const unsigned long long items = static_cast<unsigned long long>(p.BH) * (d / 8);
