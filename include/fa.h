@@ -241,8 +241,8 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, c
  * from the codes on the tensor cores' 8-bit path (exact products, fp32 sums) with
  * q_scale·k_scale folded into the softmax's exponent factor. V stays bf16 and P is rounded
  * to bf16 as in fa_fwd, so the output carries the bf16 path's error on the quantised
- * inputs. Low-precision modes are the direction step V3 of "内核案例研究：Flash Attention"
- * points to ("最近在 V3 版本中").
+ * inputs. Low-precision modes are the direction the section on versions V2 and V3 of
+ * "内核案例研究：Flash Attention" ("块稀疏注意力 V2 和 V3") points to.
  *
  *   q8, k8           : const uint8*, [B, H, T, d] e4m3 codes, device memory, 16-byte aligned
  *   q_scale, k_scale : finite and > 0

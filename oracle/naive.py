@@ -36,7 +36,7 @@ with respect to Q, K and V for an upstream gradient dO, written out by the chain
     dV = Pᵀ·dO,   dP = dO·Vᵀ,   dS_ij = P_ij·(dP_ij − Σ_k P_ik·dP_ik),
     dQ = scale·dS·K,   dK = scale·dSᵀ·Q.
 
-[HW-FA] step ④ ("can this kernel train?") says the forward keeps only the per-row
+[HW-FA] step ④ (its part on training) says the forward keeps only the per-row
 logsumexp so that the backward can recompute S and P block by block, and [FA-tiling]
 §2.2 (FlashAttention core ideas, ijyty.com: backward recomputation, per-block gradients
 summed into the global gradient). Neither page prints a backward formula, so this is the
