@@ -143,13 +143,40 @@ TRAFFIC_RECORDS = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source with comments removed and whitespace runs collapsed, string and
+    character literals kept as written: edits to comments or layout do not change it."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_sha256(which: str = "fwd") -> str:
+    """Hash of the code (comments and layout excluded) of the sources a pass compiles."""
     import hashlib
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[which]:
         h.update(name.encode())
-        with open(os.path.join(ROOT, "exact_attention_23_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "exact_attention_23_gb300", "csrc", name),
+                  encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()
 
 

@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     teardown();
   } else {
     // ---------------------------------------------------------------- compute (warps 0-7)
-    constexpr int NC = C::kNC;        // query columns of this warpgroup per tile (64 or 32)
+    constexpr int NC = C::kNC;        // query columns of this warpgroup per tile (32)
     const int g = warp >> 2;          // columns NC·g .. NC·g + NC − 1 of each tile
     const int qd = warp & 3;
     const int r = qd * 32 + lane;     // key row within the tile = TMEM lane
