@@ -39,9 +39,8 @@ cudaError_t launch_decode(const DecodeParams& p, int d, unsigned combine_grid,
                 : launch_pdl(fa_decode_kernel<128>, grid, kDecBlock, dec_smem_bytes<128>(), stream,
                              p);
   if (e != cudaSuccess || p.n_splits <= 1) return e;
-  // one merge thread per (row, 8 columns)
-  const unsigned long long items = static_cast<unsigned long long>(p.BH) * (d / 8);
-  const unsigned need = static_cast<unsigned>((items + 255) / 256);
+  // one merge warp per row, 8 warps per block
+  const unsigned need = static_cast<unsigned>((static_cast<unsigned long long>(p.BH) + 7) / 8);
   const unsigned cg = need < combine_grid ? need : combine_grid;
   const float* op = p.o_part;
   const float* lp = p.lse_part;

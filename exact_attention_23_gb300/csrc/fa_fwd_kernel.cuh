@@ -766,49 +766,90 @@ __global__ void __launch_bounds__(kThreads, 1)
 // w_s = exp(LSE_s − M), O = Σ w_s·O_s / Σ w_s (bf16) and LSE = M + ln Σ w_s; a row that no
 // range saw gets O = 0 and LSE = −∞. This is the merge of results over disjoint key blocks
 // that the first FlashAttention's outer K/V loop needed ("手写 FlashAttention", step ③),
-// used here to spread one query tile's keys over several CTAs. One thread per (row, 8
-// columns); rows = B·H·Tq.
+// used here to spread one query tile's keys over several CTAs. rows = B·H·Tq.
+//
+// One warp per row (grid-stride over rows), lane l owning columns l·D/32 … (l+1)·D/32 − 1.
+// The lanes read the ranges' LSEs side by side and agree on M and Σ w_s with shuffles; the
+// partial rows are then read eight ranges at a time, all loads in flight together. The
+// merge sits between a kernel and the caller's next one, so its latency, not its bytes,
+// is what it costs.
 template <int D>
 __global__ void __launch_bounds__(256) fa_fwd_combine_kernel(const float* __restrict__ o_part,
                                                              const float* __restrict__ lse_part,
                                                              __nv_bfloat16* __restrict__ o,
                                                              float* __restrict__ lse,
                                                              int n_splits, int rows) {
-  constexpr int L = D / 8;
+  constexpr int C = D / 32;  // columns per lane: 2 or 4
   // Launched as a programmatic dependent of the kernel that wrote the partials.
   pdl_wait();
   pdl_launch_dependents();
-  const size_t total = static_cast<size_t>(rows) * L;
-  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
-  for (size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += stride) {
-    const size_t row = idx / L;
-    const int c8 = static_cast<int>(idx % L);
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       row < rows; row += warps) {
     float m = -INFINITY;
-    for (int s = 0; s < n_splits; ++s) m = fmaxf(m, lse_part[static_cast<size_t>(s) * rows + row]);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int s = lane; s < n_splits; s += 32)
+      m = fmaxf(m, lse_part[static_cast<size_t>(s) * rows + row]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float acc[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c] = 0.f;
     float wsum = 0.f;
     if (m != -INFINITY) {
-      for (int s = 0; s < n_splits; ++s) {
-        const float ls = lse_part[static_cast<size_t>(s) * rows + row];
-        if (ls == -INFINITY) continue;
-        const float w = expf(ls - m);
-        wsum += w;
-        const float4* src = reinterpret_cast<const float4*>(
-            o_part + (static_cast<size_t>(s) * rows + row) * D + c8 * 8);
-        const float4 a = src[0], b = src[1];
-        acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-        acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+      for (int base = 0; base < n_splits; base += 32) {
+        const int cnt = min(32, n_splits - base);
+        // lane l: the weight of range base + l (0 for a range that saw no key)
+        float wl = 0.f;
+        if (lane < cnt) {
+          const float ls = lse_part[static_cast<size_t>(base + lane) * rows + row];
+          wl = (ls == -INFINITY) ? 0.f : expf(ls - m);
+        }
+        wsum += wl;
+        const float* src = o_part + (static_cast<size_t>(base) * rows + row) * D + lane * C;
+        const size_t step = static_cast<size_t>(rows) * D;
+        for (int j0 = 0; j0 < cnt; j0 += 8) {
+          float x[8][C];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (j0 + j < cnt) {
+              if constexpr (C == 2) {
+                const float2 t = *reinterpret_cast<const float2*>(src + (j0 + j) * step);
+                x[j][0] = t.x;
+                x[j][1] = t.y;
+              } else {
+                const float4 t = *reinterpret_cast<const float4*>(src + (j0 + j) * step);
+                x[j][0] = t.x;
+                x[j][1] = t.y;
+                x[j][2] = t.z;
+                x[j][3] = t.w;
+              }
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float w = __shfl_sync(0xffffffffu, wl, (j0 + j) & 31);
+            if (j0 + j < cnt) {
+#pragma unroll
+              for (int c = 0; c < C; ++c) acc[c] = fmaf(w, x[j][c], acc[c]);
+            }
+          }
+        }
       }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    uint4 out;
-    out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    out.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-    out.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    *reinterpret_cast<uint4*>(o + row * D + c8 * 8) = out;
-    if (c8 == 0) lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+    __nv_bfloat16* dst = o + static_cast<size_t>(row) * D + lane * C;
+    if constexpr (C == 2) {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    } else {
+      uint2 out;
+      out.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      out.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      *reinterpret_cast<uint2*>(dst) = out;
+    }
+    if (lane == 0) lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
   }
 }
 
