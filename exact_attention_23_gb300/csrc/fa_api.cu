@@ -156,7 +156,8 @@ int dense_forward(const void* q, const void* k, const void* v, void* o, float* l
              encode_map_e4m3(enc, &a.tm_k, k, T, d, static_cast<int>(BH)))
           : (encode_map(enc, &a.tm_q, q, T, d, static_cast<int>(BH)) &&
              encode_map(enc, &a.tm_k, k, T, d, static_cast<int>(BH)));
-  if (!maps_ok || !encode_map(enc, &a.tm_v, v, T, d, static_cast<int>(BH)))
+  if (!maps_ok || !encode_map(enc, &a.tm_v, v, T, d, static_cast<int>(BH)) ||
+      !encode_map(enc, &a.tm_o, o, T, d, static_cast<int>(BH), 32))
     return FA_ERR_INVALID_ARG;
   a.p.o = static_cast<__nv_bfloat16*>(o);
   a.p.lse = lse;
@@ -172,7 +173,8 @@ int dense_forward(const void* q, const void* k, const void* v, void* o, float* l
   // All heads interleaved in one cost-sorted list. (Limiting the interleave to the heads
   // whose K/V fit in L2 cut DRAM reads 2.6x at T = 16384 but measured 7-8 % slower: the
   // re-reads cost no time at < 20 % of HBM bandwidth, the coarser balance did.)
-  a.p.head_group = static_cast<int>(BH);
+  a.p.div_bh = fa::FastDiv::make(static_cast<uint32_t>(BH));
+  a.p.div_splits = fa::FastDiv::make(1u);
   a.p.tiles_per_cta = tiles;
   a.p.n_kv = static_cast<int>(n_qt);
   a.p.scale_log2 = scale_log2;

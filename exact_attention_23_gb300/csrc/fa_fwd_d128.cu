@@ -19,7 +19,7 @@ static cudaError_t launch_one(const FwdLaunch& a) {
     if (e != cudaSuccess) return e;
     done[dev / 64].fetch_or(bit, std::memory_order_acq_rel);
   }
-  return launch_pdl(fn, a.grid, kThreads, smem, a.stream, a.tm_q, a.tm_k, a.tm_v, a.p);
+  return launch_pdl(fn, a.grid, kThreads, smem, a.stream, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
 }
 
 cudaError_t launch_fwd_d128(const FwdLaunch& a, bool causal) {

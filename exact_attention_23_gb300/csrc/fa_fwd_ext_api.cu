@@ -85,7 +85,8 @@ int launch_general(const GenArgs& g, int sms) {
   a.p = fa::FwdParams{};
   if (!encode_map(enc, &a.tm_q, g.q, g.Tq, g.d, static_cast<int>(BH)) ||
       !encode_map(enc, &a.tm_k, g.k, g.Tk, g.d, static_cast<int>(BH)) ||
-      !encode_map(enc, &a.tm_v, g.v, g.Tk, g.d, static_cast<int>(BH)))
+      !encode_map(enc, &a.tm_v, g.v, g.Tk, g.d, static_cast<int>(BH)) ||
+      !encode_map(enc, &a.tm_o, g.o, g.Tq, g.d, static_cast<int>(BH), 32))
     return FA_ERR_INVALID_ARG;
   // Key ranges of equal length in K tiles; no range is empty.
   const long long per = (n_kt + g.splits - 1) / g.splits;
@@ -104,7 +105,7 @@ int launch_general(const GenArgs& g, int sms) {
   a.p.total_units = static_cast<int>(n_units * splits * BH);
   a.p.n_kv = static_cast<int>(n_kt);
   a.p.tiles_per_cta = tiles;
-  a.p.head_group = static_cast<int>(BH);
+  a.p.div_bh = fa::FastDiv::make(static_cast<uint32_t>(BH));
   a.p.scale_log2 = static_cast<float>(static_cast<double>(g.scale) * 1.4426950408889634074);
   a.p.timeout_ns = g.timeout_ns ? g.timeout_ns : 2000000000ull;
   a.p.flags = 0u;
@@ -112,6 +113,7 @@ int launch_general(const GenArgs& g, int sms) {
   a.p.n_qt = static_cast<int>(n_qt);
   a.p.kv_off = g.Tk - g.Tq;
   a.p.n_splits = splits;
+  a.p.div_splits = fa::FastDiv::make(static_cast<uint32_t>(splits));
   a.p.kt_per_split = static_cast<int>(per);
   a.p.bmask = g.bmask;
   a.p.bmask_heads = g.mask_heads;

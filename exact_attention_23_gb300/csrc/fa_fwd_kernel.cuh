@@ -69,7 +69,13 @@ struct Cfg {
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQBufs * 2 * kQKTileBytes;
   static constexpr int kVOff = kKOff + kStages * kQKTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  // D = 64: a 128-row output tile per Q tile, staged here in the 128-byte-swizzled layout of
+  // the O tensor map and written by one TMA store. (Written row by row from registers,
+  // every warp store touches 32 rows, and the stores of an epilogue held the warpgroup's
+  // next barrier poll back by about a thousand cycles.) D = 128 has no room for it.
+  static constexpr bool kTmaO = (D == 64);
+  static constexpr int kOOff = kVOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kOOff + (kTmaO ? 2 * kTileBytes : 0);
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + 1 KB alignment slack
   // Tensor-memory columns (see the layout at the top of this file).
   static constexpr bool kSepP = (D == 64);
@@ -98,6 +104,22 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
+// Division of 32-bit unsigned numerators by a fixed divisor d ≥ 1 without a divide: with
+// m = ⌈2⁶⁴ / d⌉, ⌊n / d⌋ = ⌊m·n / 2⁶⁴⌋ for every n < 2³² (Lemire, Kaser and Kurz, "Faster
+// remainder by direct computation", 2019, theorem 1). d = 1 is taken apart (m would not fit).
+struct FastDiv {
+  uint64_t m;
+  uint32_t d;
+  static FastDiv make(uint32_t d) { return FastDiv{d > 1u ? ~0ull / d + 1ull : 0ull, d}; }
+  __host__ __device__ __forceinline__ uint32_t div(uint32_t n) const {
+#ifdef __CUDA_ARCH__
+    return d == 1u ? n : static_cast<uint32_t>(__umul64hi(m, n));
+#else
+    return d == 1u ? n : static_cast<uint32_t>((static_cast<unsigned __int128>(m) * n) >> 64);
+#endif
+  }
+};
+
 struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
@@ -108,7 +130,8 @@ struct FwdParams {
   int total_units;    // n_units · BH
   int n_kv;           // ceil(T/128): K/V tiles, also Q tiles
   int tiles_per_cta;  // 2 (ping-pong pair) or 1 (short sequences: more CTAs)
-  int head_group;     // heads whose units are interleaved (their K/V fit in L2 together)
+  FastDiv div_bh;     // division by BH
+  FastDiv div_splits; // division by n_splits (general form)
   float scale_log2;   // scale · log2(e)
   uint64_t timeout_ns;
   uint32_t flags;
@@ -126,10 +149,9 @@ struct FwdParams {
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
-// One work unit. Heads are taken in groups small enough for their K/V to stay in L2
-// together; within a group, units are numbered heaviest first (under the causal mask the
-// cost of a Q-tile pair grows with its position), all heads of the group at one position
-// together. CTA c takes the units of round r = 0, 1, 2, ... at position c in even rounds
+// One work unit. Units are numbered heaviest first (under the causal mask the cost of a
+// Q-tile pair grows with its position), all heads at one position together. CTA c takes
+// the units of round r = 0, 1, 2, ... at position c in even rounds
 // and G−1−c in odd rounds (G = grid size). Over a list sorted by cost this zig-zag gives
 // every CTA nearly the same total work without any shared counter.
 //
@@ -163,10 +185,11 @@ __device__ __forceinline__ Unit unit_of(const FwdParams& p, int L) {
   Unit u;
   if constexpr (GEN) {
     // bh fastest, then key range, then query unit (no cost order: ranges are balanced)
-    u.bh = L % p.BH;
-    const int rest = L / p.BH;
-    u.split = rest % p.n_splits;
-    u.qt0 = (rest / p.n_splits) * p.tiles_per_cta;
+    const int rest = static_cast<int>(p.div_bh.div(static_cast<uint32_t>(L)));
+    u.bh = L - rest * p.BH;
+    const int qu = static_cast<int>(p.div_splits.div(static_cast<uint32_t>(rest)));
+    u.split = rest - qu * p.n_splits;
+    u.qt0 = qu * p.tiles_per_cta;
     u.kb = u.split * p.kt_per_split;
     u.ke = min(p.n_kv, u.kb + p.kt_per_split);
     u.mh = (p.bmask_heads == 1) ? 0 : u.bh;
@@ -188,12 +211,9 @@ __device__ __forceinline__ Unit unit_of(const FwdParams& p, int L) {
   u.kb = 0;
   u.split = 0;
   u.mh = 0;
-  const int per_group = p.n_units * p.head_group;
-  const int grp = L / per_group;
-  const int within = L - grp * per_group;
-  const int gsize = min(p.head_group, p.BH - grp * p.head_group);
-  u.bh = grp * p.head_group + within % gsize;
-  const int idx = p.n_units - 1 - within / gsize;
+  const int pos = static_cast<int>(p.div_bh.div(static_cast<uint32_t>(L)));
+  u.bh = L - pos * p.BH;
+  const int idx = p.n_units - 1 - pos;
   u.qt0 = idx * p.tiles_per_cta;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -233,7 +253,8 @@ __device__ __forceinline__ bool tile_active(const FwdParams& p, const Unit& u, i
 template <int D, bool CAUSAL, bool GEN = false, bool QK8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FwdParams p) {
   using C = Cfg<D, QK8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -292,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
+      if (C::kTmaO) tma_prefetch_desc(&tm_o);
     }
     const uint64_t keep = policy_evict_last();  // K/V are re-read by this head's other Q tiles
     const bool load_q = (p.flags & kFlagStarveQ) == 0u;
@@ -731,18 +753,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const bool empty = GEN && !(l > 0.0f);  // general form: the row saw no key
         const float inv_l = empty ? 0.0f : 1.0f / l;
+        if (C::kTmaO && !partial) {
+          // Each warp stages its 32 rows in its own 4 KB slice, 16-byte chunk c of row r at
+          // position c ^ (r mod 8) (the map's 128-byte swizzle; conflict-free), and its lane
+          // 0 stores them as one 64 × 32 box; rows past the sequence are not written. The
+          // warp's previous store from the slice (one unit back) must have read it out.
+          const int r0 = qt * kBlockM + quad * 32;
+          uint8_t* slice = smem + C::kOOff + wg * C::kTileBytes + quad * 4096;
+          const uint32_t ob = smem_u32(slice) + lane * 128;
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(t_o + c0, r);
-          tmem_ld_wait();
-          reg_fence32(r);
-          write_row(r, c0, inv_l);
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(t_o + c0, r);
+            tmem_ld_wait();
+            reg_fence32(r);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int ch = c0 / 8 + t;
+              st_shared_v4(ob + ((ch ^ (lane & 7)) << 4),
+                           pack_bf16x2(u2f(r[8 * t]) * inv_l, u2f(r[8 * t + 1]) * inv_l),
+                           pack_bf16x2(u2f(r[8 * t + 2]) * inv_l, u2f(r[8 * t + 3]) * inv_l),
+                           pack_bf16x2(u2f(r[8 * t + 4]) * inv_l, u2f(r[8 * t + 5]) * inv_l),
+                           pack_bf16x2(u2f(r[8 * t + 6]) * inv_l, u2f(r[8 * t + 7]) * inv_l));
+            }
+          }
+          // O_i has been read: the next unit's first P·V may overwrite it.
+          tc_fence_before_sync();
+          fence_proxy_async_smem();  // the staged rows, visible to the TMA engine
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars->o_free[wg]);
+            if (r0 < p.T) {
+              tma_store_3d(&tm_o, slice, 0, r0, u.bh);
+              bulk_commit_group();
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(t_o + c0, r);
+            tmem_ld_wait();
+            reg_fence32(r);
+            write_row(r, c0, inv_l);
+          }
+          // O_i has been read: the next unit's first P·V may overwrite it.
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->o_free[wg]);
         }
-        // O_i has been read: the next unit's first P·V may overwrite it.
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->o_free[wg]);
         write_lse(empty ? -INFINITY : (m_ref + log2f(l)) * 0.69314718055994530942f);
         FA_TRACE(26 + wg, 0);
       } else {
@@ -751,6 +812,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         write_lse(__uint_as_float(0x7FC00000u));
       }
     }
+    // The output rows' TMA stores must have read their shared-memory source before the
+    // CTA exits (their global writes complete with the grid).
+    if (C::kTmaO && lane == 0) bulk_wait_group_read0();
   }
 
   tc_fence_before_sync();

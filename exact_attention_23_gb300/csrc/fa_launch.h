@@ -34,6 +34,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, 
 
 struct FwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_o;  // the output, boxes of 64 columns × 32 rows (one warp's rows)
   FwdParams p;
   unsigned grid;
   cudaStream_t stream;
