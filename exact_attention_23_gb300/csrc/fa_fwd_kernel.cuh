@@ -75,7 +75,9 @@ struct Cfg {
   // next barrier poll back by about a thousand cycles.) D = 128 has no room for it.
   static constexpr bool kTmaO = (D == 64);
   static constexpr int kOOff = kVOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kOOff + (kTmaO ? 2 * kTileBytes : 0);
+  // D = 64: each softmax thread's deferred epilogue (l, m, first row of its warp, head).
+  static constexpr int kPendOff = kOOff + (kTmaO ? 2 * kTileBytes : 0);
+  static constexpr int kBarOff = kPendOff + (kTmaO ? 2 * kBlockM * 16 : 0);
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + 1 KB alignment slack
   // Tensor-memory columns (see the layout at the top of this file).
   static constexpr bool kSepP = (D == 64);
@@ -522,6 +524,152 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     int gs = 0;     // S_i consumed (= P_i produced) so far over this CTA's units
     bool ok = true;
+    // Where a unit's rows go: the bf16 output (row_idx; r0 = the warp's first row, for the
+    // TMA store) and LSE, or (general form with several key ranges) the fp32 partial row
+    // and LSE of its range.
+    struct RowOut {
+      size_t row_idx, part_idx;
+      int r0, bh;
+      bool in_range, partial;
+    };
+    // Writes 32 output columns from c0 directly: fp32 scaled by mul (partial) or bf16.
+    auto write_row = [&](const RowOut& w, const uint32_t* r, int c0, float mul) {
+      if (!w.in_range) return;
+      if (w.partial) {
+        float4* prow = reinterpret_cast<float4*>(p.o_part + w.part_idx * D + c0);
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          prow[t] = make_float4(u2f(r[4 * t]) * mul, u2f(r[4 * t + 1]) * mul,
+                                u2f(r[4 * t + 2]) * mul, u2f(r[4 * t + 3]) * mul);
+      } else {
+        uint4* orow = reinterpret_cast<uint4*>(p.o + w.row_idx * D);
+        uint32_t ob[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) ob[t] = pack_bf16x2(u2f(r[2 * t]) * mul, u2f(r[2 * t + 1]) * mul);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          orow[c0 / 8 + t] = make_uint4(ob[4 * t], ob[4 * t + 1], ob[4 * t + 2], ob[4 * t + 3]);
+      }
+    };
+    auto write_lse = [&](const RowOut& w, float v) {
+      if (!w.in_range) return;
+      if (w.partial) p.lse_part[w.part_idx] = v;
+      else p.lse[w.row_idx] = v;
+    };
+    // A row that saw no key (general form: O = 0, LSE = −∞) or a failed unit (NaN).
+    auto write_const_row = [&](const RowOut& w, uint32_t bits) {
+      if (!w.in_range) return;
+      if (w.partial) {
+        float4* prow = reinterpret_cast<float4*>(p.o_part + w.part_idx * D);
+        const float f = u2f(bits);
+#pragma unroll
+        for (int t = 0; t < D / 4; ++t) prow[t] = make_float4(f, f, f, f);
+      } else {
+        uint4* orow = reinterpret_cast<uint4*>(p.o + w.row_idx * D);
+        const uint32_t b2 = pack_bf16x2(u2f(bits), u2f(bits));
+#pragma unroll
+        for (int t = 0; t < D / 8; ++t) orow[t] = make_uint4(b2, b2, b2, b2);
+      }
+    };
+    auto fail_rows = [&](const RowOut& w) {
+      write_const_row(w, 0x7FC00000u);
+      write_lse(w, __uint_as_float(0x7FC00000u));
+    };
+    auto lse_of = [&](float l, float m) {
+      return (GEN && !(l > 0.0f)) ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f;
+    };
+    auto inv_of = [&](float l) { return (GEN && !(l > 0.0f)) ? 0.0f : 1.0f / l; };
+    // O_i, already read into registers (D = 64), to the output: each warp stages its 32
+    // rows in its own 4 KB slice, 16-byte chunk c of row r at position c ^ (r mod 8) (the
+    // map's 128-byte swizzle; conflict-free), and its lane 0 stores them as one 64 × 32
+    // box; rows past the sequence are not written. The warp's previous store from the
+    // slice (one unit back) must have read it out first.
+    auto store_o = [&](const RowOut& w, const uint32_t* o, float l, float m) {
+      const float inv_l = inv_of(l);
+      if (C::kTmaO && !w.partial) {
+        uint8_t* slice = smem + C::kOOff + wg * C::kTileBytes + quad * 4096;
+        const uint32_t ob = smem_u32(slice) + lane * 128;
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+#pragma unroll
+        for (int ch = 0; ch < D / 8; ++ch)
+          st_shared_v4(ob + ((ch ^ (lane & 7)) << 4),
+                       pack_bf16x2(u2f(o[8 * ch]) * inv_l, u2f(o[8 * ch + 1]) * inv_l),
+                       pack_bf16x2(u2f(o[8 * ch + 2]) * inv_l, u2f(o[8 * ch + 3]) * inv_l),
+                       pack_bf16x2(u2f(o[8 * ch + 4]) * inv_l, u2f(o[8 * ch + 5]) * inv_l),
+                       pack_bf16x2(u2f(o[8 * ch + 6]) * inv_l, u2f(o[8 * ch + 7]) * inv_l));
+        fence_proxy_async_smem();  // the staged rows, visible to the TMA engine
+        __syncwarp();
+        if (lane == 0 && w.r0 < p.T) {
+          tma_store_3d(&tm_o, slice, 0, w.r0, w.bh);
+          bulk_commit_group();
+        }
+      } else {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) write_row(w, o + c0, c0, inv_l);
+      }
+      write_lse(w, lse_of(l, m));
+    };
+    // Reads O_i (after its last P·V) into registers and releases it to the next unit's
+    // first P·V.
+    auto read_o = [&](uint32_t* o) {
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) tmem_ld32(t_o + c0, o + c0);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) reg_fence32(o + c0);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->o_free[wg]);
+    };
+    // D = 64 defers a unit's epilogue into this tile's first step of its next unit: that
+    // step's S load, max and exponentials run while the unit's last P·V finishes, its P is
+    // stored as soon as that P·V is done, and only then is O read out and written. (Run
+    // at once, the epilogue and the next unit's set-up, code that runs once per unit, sat
+    // between the two P·V products on the tensor core.) D = 128 keeps it immediate: its
+    // O would need 128 more registers.
+    // The pending unit's l, m and output position wait in shared memory (this thread's
+    // 16-byte record), not in registers the step loop needs. The fp32 partial rows of the
+    // general form keep the immediate epilogue.
+    const bool defer = C::kTmaO && !(GEN && p.n_splits > 1);
+    bool pend = false;
+    float4* const prec = reinterpret_cast<float4*>(smem + C::kPendOff) + wg * kBlockM + row;
+    auto park = [&](const RowOut& w, float l, float m) {
+      *prec = make_float4(l, m, __int_as_float(w.r0), __int_as_float(w.bh));
+      pend = true;
+    };
+    auto parked = [&](float& l, float& m) {
+      const float4 v = *prec;
+      l = v.x;
+      m = v.y;
+      const int r0 = __float_as_int(v.z), bh = __float_as_int(v.w);
+      const int q_row = r0 + lane;
+      return RowOut{static_cast<size_t>(bh) * static_cast<size_t>(p.T) + static_cast<size_t>(q_row),
+                    0, r0, bh, q_row < p.T, false};
+    };
+    auto fail_pending = [&]() {
+      float l, m;
+      fail_rows(parked(l, m));
+      pend = false;
+    };
+    // Finishes the pending unit once its last P·V is done (already waited for when
+    // `waited`).
+    auto flush_pending = [&](bool waited) {
+      const bool good = waited || (ok && mbar_wait_warp(&bars->pv_done[wg], (gs - 1) & 1, wc));
+      if (good) {
+        if (!waited) tc_fence_after_sync();
+        uint32_t o[D];
+        read_o(o);
+        float l, m;
+        const RowOut w = parked(l, m);
+        store_o(w, o, l, m);
+        pend = false;
+      } else {
+        ok = false;
+        fail_pending();
+      }
+    };
+
     for (int r = 0; r * grid < p.total_units; ++r) {
       const int L = unit_index(r, cta, grid);
       if (L >= p.total_units) continue;
@@ -532,61 +680,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q_row = qt * kBlockM + row;
       const bool tile_exists = wg < p.tiles_per_cta && qt * kBlockM < p.T;
       if (n == 0 && !(GEN && tile_exists)) continue;
-      const size_t row_idx = static_cast<size_t>(u.bh) * static_cast<size_t>(p.T) +
-                             static_cast<size_t>(q_row);
-      const bool in_range = q_row < p.T;
-      uint4* orow = reinterpret_cast<uint4*>(p.o + row_idx * D);
-      // General form with several key ranges: this unit's fp32 partial row.
-      const bool partial = GEN && p.n_splits > 1;
-      const size_t part_idx =
-          (static_cast<size_t>(u.split) * p.BH + u.bh) * static_cast<size_t>(p.T) + q_row;
-      // Writes an output row: fp32 values scaled by mul (partial) or bf16 (final).
-      auto write_row = [&](const uint32_t* r, int c0, float mul) {
-        if (!in_range) return;
-        if (partial) {
-          float4* prow = reinterpret_cast<float4*>(p.o_part + part_idx * D + c0);
-#pragma unroll
-          for (int t = 0; t < 8; ++t)
-            prow[t] = make_float4(u2f(r[4 * t]) * mul, u2f(r[4 * t + 1]) * mul,
-                                  u2f(r[4 * t + 2]) * mul, u2f(r[4 * t + 3]) * mul);
-        } else {
-          uint32_t ob[16];
-#pragma unroll
-          for (int t = 0; t < 16; ++t)
-            ob[t] = pack_bf16x2(u2f(r[2 * t]) * mul, u2f(r[2 * t + 1]) * mul);
-#pragma unroll
-          for (int t = 0; t < 4; ++t)
-            orow[c0 / 8 + t] = make_uint4(ob[4 * t], ob[4 * t + 1], ob[4 * t + 2], ob[4 * t + 3]);
-        }
-      };
-      auto write_lse = [&](float v) {
-        if (!in_range) return;
-        if (partial) p.lse_part[part_idx] = v;
-        else p.lse[row_idx] = v;
-      };
-      // A row that saw no key (general form: O = 0, LSE = −∞) or a failed unit (NaN).
-      auto write_const_row = [&](uint32_t bits) {
-        if (!in_range) return;
-        if (partial) {
-          float4* prow = reinterpret_cast<float4*>(p.o_part + part_idx * D);
-          const float f = u2f(bits);
-#pragma unroll
-          for (int t = 0; t < D / 4; ++t) prow[t] = make_float4(f, f, f, f);
-        } else {
-          const uint32_t b2 = pack_bf16x2(u2f(bits), u2f(bits));
-#pragma unroll
-          for (int t = 0; t < D / 8; ++t) orow[t] = make_uint4(b2, b2, b2, b2);
-        }
-      };
+      const RowOut cur{static_cast<size_t>(u.bh) * static_cast<size_t>(p.T) +
+                           static_cast<size_t>(q_row),
+                       (static_cast<size_t>(u.split) * p.BH + u.bh) * static_cast<size_t>(p.T) +
+                           q_row,
+                       qt * kBlockM + quad * 32, u.bh, q_row < p.T, GEN && p.n_splits > 1};
       if (!ok) {
         // A wait gave up earlier: mark every row this warpgroup owns as failed.
-        write_const_row(0x7FC00000u);
-        write_lse(__uint_as_float(0x7FC00000u));
+        if (pend) fail_pending();
+        fail_rows(cur);
         continue;
       }
       if (n == 0) {  // general form: this tile uses no K tile of the range
-        write_const_row(0u);
-        write_lse(-INFINITY);
+        if (pend) flush_pending(false);
+        write_const_row(cur, 0u);
+        write_lse(cur, -INFINITY);
         continue;
       }
 
@@ -744,74 +852,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_full[wg]);
         FA_TRACE(22 + wg, j);
+        // (j = 0) The previous unit's last P·V was the one waited for above: its O_i is
+        // final. Read it out (releasing O_i to this unit's first P·V), then write it.
+        if (C::kTmaO && pend) flush_pending(true);
+      }
+      if (!ok) {
+        if (pend) fail_pending();
+        fail_rows(cur);
+        continue;
+      }
+      if (defer) {
+        park(cur, l, m_ref);
+        continue;
       }
 
-      // Epilogue: O / l and the logsumexp, once this unit's last P·V is done.
-      const bool good = ok && mbar_wait_warp(&bars->pv_done[wg], (gs - 1) & 1, wc);
+      // Epilogue at once (D = 128): O / l and the logsumexp, once this unit's last P·V is
+      // done; O is read 32 columns at a time.
+      const bool good = mbar_wait_warp(&bars->pv_done[wg], (gs - 1) & 1, wc);
       FA_TRACE(24 + wg, 0);
       if (good) {
         tc_fence_after_sync();
-        const bool empty = GEN && !(l > 0.0f);  // general form: the row saw no key
-        const float inv_l = empty ? 0.0f : 1.0f / l;
-        if (C::kTmaO && !partial) {
-          // Each warp stages its 32 rows in its own 4 KB slice, 16-byte chunk c of row r at
-          // position c ^ (r mod 8) (the map's 128-byte swizzle; conflict-free), and its lane
-          // 0 stores them as one 64 × 32 box; rows past the sequence are not written. The
-          // warp's previous store from the slice (one unit back) must have read it out.
-          const int r0 = qt * kBlockM + quad * 32;
-          uint8_t* slice = smem + C::kOOff + wg * C::kTileBytes + quad * 4096;
-          const uint32_t ob = smem_u32(slice) + lane * 128;
-          if (lane == 0) bulk_wait_group_read0();
-          __syncwarp();
+        const float inv_l = inv_of(l);
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(t_o + c0, r);
-            tmem_ld_wait();
-            reg_fence32(r);
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const int ch = c0 / 8 + t;
-              st_shared_v4(ob + ((ch ^ (lane & 7)) << 4),
-                           pack_bf16x2(u2f(r[8 * t]) * inv_l, u2f(r[8 * t + 1]) * inv_l),
-                           pack_bf16x2(u2f(r[8 * t + 2]) * inv_l, u2f(r[8 * t + 3]) * inv_l),
-                           pack_bf16x2(u2f(r[8 * t + 4]) * inv_l, u2f(r[8 * t + 5]) * inv_l),
-                           pack_bf16x2(u2f(r[8 * t + 6]) * inv_l, u2f(r[8 * t + 7]) * inv_l));
-            }
-          }
-          // O_i has been read: the next unit's first P·V may overwrite it.
-          tc_fence_before_sync();
-          fence_proxy_async_smem();  // the staged rows, visible to the TMA engine
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&bars->o_free[wg]);
-            if (r0 < p.T) {
-              tma_store_3d(&tm_o, slice, 0, r0, u.bh);
-              bulk_commit_group();
-            }
-          }
-        } else {
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(t_o + c0, r);
-            tmem_ld_wait();
-            reg_fence32(r);
-            write_row(r, c0, inv_l);
-          }
-          // O_i has been read: the next unit's first P·V may overwrite it.
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->o_free[wg]);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(t_o + c0, r);
+          tmem_ld_wait();
+          reg_fence32(r);
+          write_row(cur, r, c0, inv_l);
         }
-        write_lse(empty ? -INFINITY : (m_ref + log2f(l)) * 0.69314718055994530942f);
+        // O_i has been read: the next unit's first P·V may overwrite it.
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_free[wg]);
+        write_lse(cur, lse_of(l, m_ref));
         FA_TRACE(26 + wg, 0);
       } else {
         ok = false;
-        write_const_row(0x7FC00000u);
-        write_lse(__uint_as_float(0x7FC00000u));
+        fail_rows(cur);
       }
     }
+    if (pend) flush_pending(false);  // the last unit's epilogue
     // The output rows' TMA stores must have read their shared-memory source before the
     // CTA exits (their global writes complete with the grid).
     if (C::kTmaO && lane == 0) bulk_wait_group_read0();
