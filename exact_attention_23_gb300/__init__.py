@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     FA_ERR_TIMEOUT,
     FA_ERR_UNSUPPORTED_DEVICE,
     FA_FLAG_TEST_STARVE_Q,
+    FA_FLAG_TEST_STARVE_LATER_Q,
     FA_OK,
     FAError,
     fa_bwd,

@@ -124,7 +124,8 @@ int dense_forward(const void* q, const void* k, const void* v, void* o, float* l
   if (B <= 0 || H <= 0 || T <= 0) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale_log2) || !(scale_log2 > 0.0f)) return FA_ERR_INVALID_ARG;
-  if ((flags & ~static_cast<unsigned>(FA_FLAG_TEST_STARVE_Q)) != 0u) return FA_ERR_INVALID_ARG;
+  if ((flags & ~static_cast<unsigned>(FA_FLAG_TEST_STARVE_Q | FA_FLAG_TEST_STARVE_LATER_Q)) != 0u)
+    return FA_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * H;
   const long long n_qt = (static_cast<long long>(T) + 127) / 128;
   const long long n_pairs = (n_qt + 1) / 2;

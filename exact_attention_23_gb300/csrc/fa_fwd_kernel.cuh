@@ -51,7 +51,8 @@ constexpr int kBlockM = 128;    // query rows per Q tile = TMEM lanes
 constexpr int kBlockN = 128;    // keys per K/V tile
 constexpr int kThreads = 352;
 constexpr float kTau = 8.0f;    // lazy rescale: O and l keep a stale max until it is 2^8 too small
-constexpr uint32_t kFlagStarveQ = 1u;  // FA_FLAG_TEST_STARVE_Q
+constexpr uint32_t kFlagStarveQ = 1u;       // FA_FLAG_TEST_STARVE_Q
+constexpr uint32_t kFlagStarveLaterQ = 2u;  // FA_FLAG_TEST_STARVE_LATER_Q
 
 template <int D, bool QK8 = false>
 struct Cfg {
@@ -319,8 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint64_t keep = policy_evict_last();  // K/V are re-read by this head's other Q tiles
     const bool load_q = (p.flags & kFlagStarveQ) == 0u;
+    const bool later_q = (p.flags & kFlagStarveLaterQ) == 0u;
     int g = 0;       // K/V steps issued so far (over this CTA's units)
     int qn = 0;      // Q tile pairs issued so far
+    int ql = 0;      // ... of which loaded (fewer only under the test flags)
     bool ok = true;
     for (int r = 0; ok && r * grid < p.total_units; ++r) {
       const int L = unit_index(r, cta, grid);
@@ -329,7 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qb = qn % C::kQBufs;
       if (qn >= C::kQBufs &&
           !mbar_wait_warp(&bars->q_empty[qb], ((qn / C::kQBufs) - 1) & 1, wc)) { ok = false; break; }
-      if (load_q && leader) {
+      const bool load = load_q && (later_q || qn == 0);
+      if (load) ++ql;
+      if (load && leader) {
         mbar_arrive_expect_tx(&bars->q_full[qb], p.tiles_per_cta * C::kQKTileBytes);
         for (int i = 0; i < p.tiles_per_cta; ++i)
 #pragma unroll
@@ -362,11 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // Drain: every copy issued must have landed before this CTA may exit.
-    if (load_q) {
-      for (int b = 0; b < C::kQBufs && b < qn; ++b) {
-        const int last = (qn - 1 - b) / C::kQBufs;  // last use of buffer b
-        mbar_wait_warp(&bars->q_full[b], last & 1, drain);
-      }
+    // (Q was loaded for the CTA's first ql units; buffer b served every kQBufs-th of them.)
+    for (int b = 0; b < C::kQBufs && b < ql; ++b) {
+      const int last = (ql - 1 - b) / C::kQBufs;  // last loaded use of buffer b
+      mbar_wait_warp(&bars->q_full[b], last & 1, drain);
     }
     for (int st = 0; st < C::kStages && st < g; ++st) {
       const int last_use = (g - 1 - st) / C::kStages;

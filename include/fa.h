@@ -83,12 +83,15 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
  *                property.
  *   timeout_ns : limit for every internal wait, in nanoseconds; 0 selects 2 s.
  *   flags      : 0 for normal use. Bit 0 (FA_FLAG_TEST_STARVE_Q) makes the kernel omit
- *                the query-tile loads so that every dependent wait runs out; it exists
- *                only to test the timeout path and produces NaN outputs.
+ *                the query-tile loads so that every dependent wait runs out; bit 1
+ *                (FA_FLAG_TEST_STARVE_LATER_Q) omits them from each CTA's second work
+ *                unit on, so that the waits run out after a first unit has finished.
+ *                Both exist only to test the timeout path and produce NaN outputs.
  *
  * Everything else as fa_fwd.
  */
 #define FA_FLAG_TEST_STARVE_Q 1u
+#define FA_FLAG_TEST_STARVE_LATER_Q 2u
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
               int T, int d, int causal, float scale, int* status, unsigned long long timeout_ns,
               unsigned int flags, void* stream);

@@ -55,6 +55,8 @@ def test_status_codes_match_header():
         assert m and int(m.group(1)) == getattr(fa, name), name
     m = re.search(r"#define\s+FA_FLAG_TEST_STARVE_Q\s+(\d+)u", text)
     assert m and int(m.group(1)) == fa.FA_FLAG_TEST_STARVE_Q
+    m = re.search(r"#define\s+FA_FLAG_TEST_STARVE_LATER_Q\s+(\d+)u", text)
+    assert m and int(m.group(1)) == fa.FA_FLAG_TEST_STARVE_LATER_Q
 
 
 # Fake, never-dereferenced device addresses: validation fails before any CUDA call.
@@ -83,7 +85,7 @@ def _call(q=A, k=A + SZ, v=A + 2 * SZ, o=A + 3 * SZ, lse=A + 4 * SZ, B=1, H=1, T
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
     (dict(scale=-0.125), fa.FA_ERR_INVALID_ARG),
-    (dict(flags=2), fa.FA_ERR_INVALID_ARG),
+    (dict(flags=4), fa.FA_ERR_INVALID_ARG),
     (dict(q=A + 8), fa.FA_ERR_MISALIGNED),
     (dict(o=A + 3 * SZ + 2), fa.FA_ERR_MISALIGNED),
     (dict(lse=A + 4 * SZ + 4), fa.FA_ERR_MISALIGNED),

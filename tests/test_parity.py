@@ -193,6 +193,32 @@ def test_timeout_path_reports_status_and_context_survives():
              "after timeout")
 
 
+def test_timeout_after_a_finished_unit_reports_status_and_context_survives():
+    """Each CTA's first work unit gets its query tiles, later units do not: the first unit
+    completes and its epilogue waits (deferred into the next unit's first step) when the
+    next unit's waits run out. The kernel must report FA_ERR_TIMEOUT, write NaN for every
+    row it owns (the finished unit's included: its epilogue is abandoned with the rest),
+    and leave the context usable. B4 H12 T4096 gives every CTA at least five units."""
+    torch = _torch()
+    import exact_attention_23_gb300 as fa
+    q, k, v = (t.cuda() for t in inputs.make_qkv(4, 12, 4096, 64, seed=46))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, lse = fa.fwd(q, k, v, causal=True, status=status, timeout_ns=20_000_000,
+                    flags=fa.FA_FLAG_TEST_STARVE_LATER_Q)
+    torch.cuda.synchronize()
+    assert int(status.item()) == fa.FA_ERR_TIMEOUT
+    assert bool(torch.isnan(lse).all()) and bool(torch.isnan(o.float()).all())
+    status.zero_()
+    o, lse = fa.fwd(q, k, v, causal=True, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rows = np.array([0, 1, 127, 128, 2047, 4095])
+    qn, kn, vn = (inputs.to_f64_numpy(t[1, 7].cpu()) for t in (q, k, v))
+    o_ref, lse_ref = oracle.attention_rows(qn, kn, vn, True, 0.125, rows)
+    _compare(o[1, 7, rows].float().cpu().double().numpy(), lse[1, 7, rows].cpu().double().numpy(),
+             o_ref, lse_ref, "after timeout")
+
+
 def test_misaligned_pointer_rejected_on_device():
     torch = _torch()
     import exact_attention_23_gb300 as fa
