@@ -79,7 +79,12 @@ struct Cfg {
   // D = 64: each softmax thread's deferred epilogue (l, m, first row of its warp, head).
   static constexpr int kPendOff = kOOff + (kTmaO ? 2 * kTileBytes : 0);
   static constexpr int kBarOff = kPendOff + (kTmaO ? 2 * kBlockM * 16 : 0);
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + 1 KB alignment slack
+  static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + 1 KB alignment slack
+  // P is stored, and P·V issued, in kPParts parts of the keys. D = 128: two halves, so the
+  // first half's P·V (four N = 128 products) runs while the second is exponentiated
+  // (measured +6 %). D = 64: one part (halves measured 15 % slower: the extra wait and
+  // commit between two short batches of N = 64 products cost more than they hide).
+  static constexpr int kPParts = (D == 128) ? 2 : 1;
   // Tensor-memory columns (see the layout at the top of this file).
   static constexpr bool kSepP = (D == 64);
   static __device__ __forceinline__ constexpr uint32_t col_s(int i) { return i ? 128u : 0u; }
@@ -97,7 +102,9 @@ struct Bars {
   uint64_t kv_empty[4]; // two arrivals per use: K released by the S issuer, V by the P·V issuer
   uint64_t s_full[2];   // S_i computed (tensor core -> softmax)
   uint64_t s_free[2];   // S_i read into registers (softmax -> S issuer); D = 64 only
-  uint64_t p_full[2];   // P_i stored, O_i rescaled if needed (softmax -> P·V issuer)
+  uint64_t p_full[2][2];  // [i][h]: part h of P_i's keys stored, O_i rescaled if needed
+                         // (softmax -> P·V issuer)
+  uint64_t pv_half[2];  // the first part of P_i·V done: those keys of P_i reusable
   uint64_t pv_done[2];  // P_i·V done: P_i reusable, O_i stable (tensor core -> softmax)
   uint64_t o_free[2];   // a unit's O_i has been read out (softmax -> P·V issuer)
   uint64_t mma_done;
@@ -105,7 +112,7 @@ struct Bars {
   uint32_t abort;
   uint32_t never;  // stays 0: abort flag of the drain waits, which must not be cut short
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 // Division of 32-bit unsigned numerators by a fixed divisor d ≥ 1 without a divide: with
 // m = ⌈2⁶⁴ / d⌉, ⌊n / d⌋ = ⌊m·n / 2⁶⁴⌋ for every n < 2³² (Lemire, Kaser and Kurz, "Faster
@@ -284,7 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->s_free[i], 4);
-      mbar_init(&bars->p_full[i], 4);
+      mbar_init(&bars->p_full[i][0], 4);
+      mbar_init(&bars->p_full[i][1], 4);
+      mbar_init(&bars->pv_half[i], 1);
       mbar_init(&bars->pv_done[i], 1);
       mbar_init(&bars->o_free[i], 4);
     }
@@ -458,19 +467,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O_i += P_i · V_st : A = P from TMEM (8 columns = 16 keys per step), B = V tile,
       // MN-major (D contiguous): 16 keys = 2048 bytes per step; next 64-wide column block
       // (leading byte offset) 16 KB away; next 8-key group (stride byte offset) 1 KB away.
-      // Committed to pv_done[i].
+      // Issued in C::kPParts parts of the keys as the softmax stores them; a first part is
+      // committed to pv_half[i], the whole to pv_done[i].
       constexpr uint32_t kIdescO = idesc_bf16(kBlockM, D, true);
       const uint32_t v_base = smem_u32(smem + C::kVOff);
-      auto issue_pv = [&](int i, int st, bool acc) {
+      auto issue_pv = [&](int i, int st, bool acc, int h) {
         if (leader) {
           const uint32_t va = v_base + st * C::kTileBytes;
+          constexpr int kPer = kBlockN / 16 / C::kPParts;  // K = 16 steps per part
 #pragma unroll
-          for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          for (int k4 = 0; k4 < kPer; ++k4) {
+            const int kk = h * kPer + k4;
             mma_ts(tmem + C::col_o(i), tmem + C::col_p(i) + kk * 8,
                    sdesc_sw128(va + kk * 2048, C::kSubBytes, 1024), kIdescO,
                    (acc || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&bars->pv_done[i]);
+          mma_commit(h == C::kPParts - 1 ? &bars->pv_done[i] : &bars->pv_half[i]);
         }
         __syncwarp();
       };
@@ -496,10 +508,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               // been read out.
               if (!mbar_wait_warp(&bars->o_free[i], (nunits[i] - 1) & 1, wc)) { ok = false; break; }
             }
-            if (!mbar_wait_warp(&bars->p_full[i], np[i] & 1, wc)) { ok = false; break; }
-            FA_TRACE(11 + i, j);
-            tc_fence_after_sync();
-            issue_pv(i, st, jt[i] > 0);
+#pragma unroll
+            for (int h = 0; h < C::kPParts; ++h) {
+              if (!mbar_wait_warp(&bars->p_full[i][h], np[i] & 1, wc)) { ok = false; break; }
+              if (h == 0) FA_TRACE(11 + i, j);
+              tc_fence_after_sync();
+              issue_pv(i, st, jt[i] > 0, h);
+            }
+            if (!ok) break;
             ++np[i];
             ++jt[i];
             FA_TRACE(14 + i, j);
@@ -803,58 +819,76 @@ __global__ void __launch_bounds__(kThreads, 1)
           rescale = true;
         }
 
-        // p = 2^(s·c − m_ref) on fp32 pairs; row sum in fp32; P kept as bf16 pairs.
+        const bool any_rescale = __any_sync(0xffffffffu, rescale);
+        bool waited = false;
+
+        // p = 2^(s·c − m_ref) on fp32 pairs; row sum in fp32; P kept as bf16 pairs. Each
+        // part of the keys is stored and signalled as soon as it is ready.
         const uint64_t c2 = f2_pack(c, c);
         // (general form: a row with no visible key so far keeps m_ref = −∞; its p are 0)
         const float m_use = (GEN && m_ref == -INFINITY) ? 0.0f : m_ref;
         const uint64_t nm2 = f2_pack(-m_use, -m_use);
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-        uint32_t pk[kBlockN / 2];
+        constexpr int kPk = kBlockN / 2 / C::kPParts;  // bf16 pairs per part
 #pragma unroll
-        for (int t = 0; t < kBlockN / 2; ++t) {
-          const uint64_t x2 = f2_fma(f2_pack(u2f(s[2 * t]), u2f(s[2 * t + 1])), c2, nm2);
-          float x0, x1;
-          f2_unpack(x2, x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          if (t & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
-          else acc0 = f2_add(acc0, f2_pack(p0, p1));
-          pk[t] = pack_bf16x2(p0, p1);
+        for (int h = 0; h < C::kPParts; ++h) {
+          uint32_t pk[kPk];
+#pragma unroll
+          for (int t2 = 0; t2 < kPk; ++t2) {
+            const int t = h * kPk + t2;
+            const uint64_t x2 = f2_fma(f2_pack(u2f(s[2 * t]), u2f(s[2 * t + 1])), c2, nm2);
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            if (t & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
+            else acc0 = f2_add(acc0, f2_pack(p0, p1));
+            pk[t2] = pack_bf16x2(p0, p1);
+          }
+          if (h == C::kPParts - 1) FA_TRACE(42 + wg, j);
+          if (h == 0 && any_rescale) {
+            // Rows whose max jumped bring their accumulated O to the new reference (rare:
+            // the reference moves only by more than τ), before any of this step's P·V. O
+            // must be stable: the previous P·V done. 16 columns at a time (the second half
+            // of S may still be live).
+            if (C::kSepP && gs > 0) {
+              if (!mbar_wait_warp(&bars->pv_done[wg], (gs - 1) & 1, wc)) { ok = false; break; }
+              tc_fence_after_sync();
+              waited = true;
+            }
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 16) {
+              uint32_t r[16];
+              tmem_ld16(t_o + c0, r);
+              tmem_ld_wait();
+              reg_fence16(r);
+#pragma unroll
+              for (int t = 0; t < 16; ++t) r[t] = __float_as_uint(u2f(r[t]) * alpha);
+              tmem_st16(t_o + c0, r);
+            }
+          }
+          if constexpr (C::kSepP) {
+            // These P_i columns are free once the matching part of the previous P_i·V is done.
+            if (gs > 0 && !waited) {
+              if (!mbar_wait_warp(h == C::kPParts - 1 ? &bars->pv_done[wg] : &bars->pv_half[wg],
+                                  (gs - 1) & 1, wc)) { ok = false; break; }
+              tc_fence_after_sync();
+            }
+          }
+#pragma unroll
+          for (int c0 = 0; c0 < kPk; c0 += 32) tmem_st32(t_p + h * kPk + c0, pk + c0);
+          tmem_st_wait();
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->p_full[wg][h]);
         }
+        if (!ok) break;
         {
           float a0, a1, b0, b1;
           f2_unpack(acc0, a0, a1);
           f2_unpack(acc1, b0, b1);
           l += (a0 + b0) + (a1 + b1);
         }
-        FA_TRACE(42 + wg, j);
-        if constexpr (C::kSepP) {
-          // P_i's columns and O_i are free once the previous P_i·V has finished.
-          if (gs > 0) {
-            if (!mbar_wait_warp(&bars->pv_done[wg], (gs - 1) & 1, wc)) { ok = false; break; }
-            tc_fence_after_sync();
-          }
-        }
-        if (__any_sync(0xffffffffu, rescale)) {
-          // Rows whose max jumped bring their accumulated O to the new reference. O is
-          // stable here (the previous P·V is done) and not read again before p_full.
-#pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(t_o + c0, r);
-            tmem_ld_wait();
-            reg_fence32(r);
-#pragma unroll
-            for (int t = 0; t < 32; ++t) r[t] = __float_as_uint(u2f(r[t]) * alpha);
-            tmem_st32(t_o + c0, r);
-          }
-        }
-        tmem_st32(t_p + 0, pk);
-        tmem_st32(t_p + 32, pk + 32);
-        tmem_st_wait();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->p_full[wg]);
         FA_TRACE(22 + wg, j);
         // (j = 0) The previous unit's last P·V was the one waited for above: its O_i is
         // final. Read it out (releasing O_i to this unit's first P·V), then write it.
