@@ -82,9 +82,11 @@ struct Cfg {
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + 1 KB alignment slack
   // P is stored, and P·V issued, in kPParts parts of the keys. D = 128: two halves, so the
   // first half's P·V (four N = 128 products) runs while the second is exponentiated
-  // (measured +6 %). D = 64: one part (halves measured 15 % slower: the extra wait and
-  // commit between two short batches of N = 64 products cost more than they hide).
+  // (measured +6 %; four quarters measured 15 % slower than halves). D = 64: one part
+  // (halves measured 15 % slower: the extra wait and commit between two short batches of
+  // N = 64 products cost more than they hide).
   static constexpr int kPParts = (D == 128) ? 2 : 1;
+  static_assert(kPParts == 1 || kPParts == 2 || kPParts == 4, "P parts (barrier arrays hold 4)");
   // Tensor-memory columns (see the layout at the top of this file).
   static constexpr bool kSepP = (D == 64);
   static __device__ __forceinline__ constexpr uint32_t col_s(int i) { return i ? 128u : 0u; }
@@ -102,9 +104,9 @@ struct Bars {
   uint64_t kv_empty[4]; // two arrivals per use: K released by the S issuer, V by the P·V issuer
   uint64_t s_full[2];   // S_i computed (tensor core -> softmax)
   uint64_t s_free[2];   // S_i read into registers (softmax -> S issuer); D = 64 only
-  uint64_t p_full[2][2];  // [i][h]: part h of P_i's keys stored, O_i rescaled if needed
-                         // (softmax -> P·V issuer)
-  uint64_t pv_half[2];  // the first part of P_i·V done: those keys of P_i reusable
+  uint64_t p_full[2][4];   // [i][h]: part h of P_i's keys stored, O_i rescaled if needed
+                          // (softmax -> P·V issuer)
+  uint64_t pv_part[2][3];  // [i][h]: parts 0..h of P_i·V done: their keys of P_i reusable
   uint64_t pv_done[2];  // P_i·V done: P_i reusable, O_i stable (tensor core -> softmax)
   uint64_t o_free[2];   // a unit's O_i has been read out (softmax -> P·V issuer)
   uint64_t mma_done;
@@ -291,9 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->s_full[i], 1);
       mbar_init(&bars->s_free[i], 4);
-      mbar_init(&bars->p_full[i][0], 4);
-      mbar_init(&bars->p_full[i][1], 4);
-      mbar_init(&bars->pv_half[i], 1);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) mbar_init(&bars->p_full[i][h], 4);
+#pragma unroll
+      for (int h = 0; h < 3; ++h) mbar_init(&bars->pv_part[i][h], 1);
       mbar_init(&bars->pv_done[i], 1);
       mbar_init(&bars->o_free[i], 4);
     }
@@ -467,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O_i += P_i · V_st : A = P from TMEM (8 columns = 16 keys per step), B = V tile,
       // MN-major (D contiguous): 16 keys = 2048 bytes per step; next 64-wide column block
       // (leading byte offset) 16 KB away; next 8-key group (stride byte offset) 1 KB away.
-      // Issued in C::kPParts parts of the keys as the softmax stores them; a first part is
-      // committed to pv_half[i], the whole to pv_done[i].
+      // Issued in C::kPParts parts of the keys as the softmax stores them; part h < last is
+      // committed to pv_part[i][h], the whole to pv_done[i].
       constexpr uint32_t kIdescO = idesc_bf16(kBlockM, D, true);
       const uint32_t v_base = smem_u32(smem + C::kVOff);
       auto issue_pv = [&](int i, int st, bool acc, int h) {
@@ -482,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    sdesc_sw128(va + kk * 2048, C::kSubBytes, 1024), kIdescO,
                    (acc || kk > 0) ? 1u : 0u);
           }
-          mma_commit(h == C::kPParts - 1 ? &bars->pv_done[i] : &bars->pv_half[i]);
+          mma_commit(h == C::kPParts - 1 ? &bars->pv_done[i] : &bars->pv_part[i][h]);
         }
         __syncwarp();
       };
@@ -870,13 +873,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (C::kSepP) {
             // These P_i columns are free once the matching part of the previous P_i·V is done.
             if (gs > 0 && !waited) {
-              if (!mbar_wait_warp(h == C::kPParts - 1 ? &bars->pv_done[wg] : &bars->pv_half[wg],
+              if (!mbar_wait_warp(h == C::kPParts - 1 ? &bars->pv_done[wg] : &bars->pv_part[wg][h],
                                   (gs - 1) & 1, wc)) { ok = false; break; }
               tc_fence_after_sync();
             }
           }
+          if constexpr (kPk >= 32) {
 #pragma unroll
-          for (int c0 = 0; c0 < kPk; c0 += 32) tmem_st32(t_p + h * kPk + c0, pk + c0);
+            for (int c0 = 0; c0 < kPk; c0 += 32) tmem_st32(t_p + h * kPk + c0, pk + c0);
+          } else {
+            tmem_st16(t_p + h * kPk, pk);
+          }
           tmem_st_wait();
           tc_fence_before_sync();
           __syncwarp();
