@@ -70,15 +70,16 @@ struct Cfg {
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQBufs * 2 * kQKTileBytes;
   static constexpr int kVOff = kKOff + kStages * kQKTileBytes;
-  // D = 64: a 128-row output tile per Q tile, staged here in the 128-byte-swizzled layout of
-  // the O tensor map and written by one TMA store. (Written row by row from registers,
-  // every warp store touches 32 rows, and the stores of an epilogue held the warpgroup's
-  // next barrier poll back by about a thousand cycles.) D = 128 has no room for it.
-  static constexpr bool kTmaO = (D == 64);
+  // Output staging: each softmax warp's 32 rows × 64 columns (4 KB, one box of the O tensor
+  // map, 128-byte swizzle) go through shared memory to one TMA store; D = 128 takes two
+  // rounds. (Written row by row from registers, every warp store touched 32 rows, and an
+  // epilogue's stores held the warp's next barrier poll back by about a thousand cycles.)
   static constexpr int kOOff = kVOff + kStages * kTileBytes;
+  static constexpr int kOBytes = 8 * 4096;
   // D = 64: each softmax thread's deferred epilogue (l, m, first row of its warp, head).
-  static constexpr int kPendOff = kOOff + (kTmaO ? 2 * kTileBytes : 0);
-  static constexpr int kBarOff = kPendOff + (kTmaO ? 2 * kBlockM * 16 : 0);
+  static constexpr bool kDefer = (D == 64);
+  static constexpr int kPendOff = kOOff + kOBytes;
+  static constexpr int kBarOff = kPendOff + (kDefer ? 2 * kBlockM * 16 : 0);
   static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + 1 KB alignment slack
   // P is stored, and P·V issued, in kPParts parts of the keys. D = 128: two halves, so the
   // first half's P·V (four N = 128 products) runs while the second is exponentiated
@@ -328,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      if (C::kTmaO) tma_prefetch_desc(&tm_o);
+      tma_prefetch_desc(&tm_o);
     }
     const uint64_t keep = policy_evict_last();  // K/V are re-read by this head's other Q tiles
     const bool load_q = (p.flags & kFlagStarveQ) == 0u;
@@ -609,8 +610,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // slice (one unit back) must have read it out first.
     auto store_o = [&](const RowOut& w, const uint32_t* o, float l, float m) {
       const float inv_l = inv_of(l);
-      if (C::kTmaO && !w.partial) {
-        uint8_t* slice = smem + C::kOOff + wg * C::kTileBytes + quad * 4096;
+      if (D == 64 && !w.partial) {
+        uint8_t* slice = smem + C::kOOff + (wg * 4 + quad) * 4096;
         const uint32_t ob = smem_u32(slice) + lane * 128;
         if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
@@ -654,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The pending unit's l, m and output position wait in shared memory (this thread's
     // 16-byte record), not in registers the step loop needs. The fp32 partial rows of the
     // general form keep the immediate epilogue.
-    const bool defer = C::kTmaO && !(GEN && p.n_splits > 1);
+    const bool defer = C::kDefer && !(GEN && p.n_splits > 1);
     bool pend = false;
     float4* const prec = reinterpret_cast<float4*>(smem + C::kPendOff) + wg * kBlockM + row;
     auto park = [&](const RowOut& w, float l, float m) {
@@ -899,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         FA_TRACE(22 + wg, j);
         // (j = 0) The previous unit's last P·V was the one waited for above: its O_i is
         // final. Read it out (releasing O_i to this unit's first P·V), then write it.
-        if (C::kTmaO && pend) flush_pending(true);
+        if (C::kDefer && pend) flush_pending(true);
       }
       if (!ok) {
         if (pend) fail_pending();
@@ -911,25 +912,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
 
-      // Epilogue at once (D = 128): O / l and the logsumexp, once this unit's last P·V is
-      // done; O is read 32 columns at a time.
+      // Epilogue at once (D = 128, and the partial rows): O / l and the logsumexp, once this
+      // unit's last P·V is done.
       const bool good = mbar_wait_warp(&bars->pv_done[wg], (gs - 1) & 1, wc);
       FA_TRACE(24 + wg, 0);
       if (good) {
         tc_fence_after_sync();
         const float inv_l = inv_of(l);
+        if (!cur.partial) {
+          // 64 columns per round through the warp's staging slice, 32 at a time from TMEM.
+          uint8_t* slice = smem + C::kOOff + (wg * 4 + quad) * 4096;
+          const uint32_t ob = smem_u32(slice) + lane * 128;
+#pragma unroll 1
+          for (int hb = 0; hb < D / 64; ++hb) {
+            if (lane == 0) bulk_wait_group_read0();  // the slice's previous store read it
+            __syncwarp();
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(t_o + c0, r);
-          tmem_ld_wait();
-          reg_fence32(r);
-          write_row(cur, r, c0, inv_l);
+            for (int half = 0; half < 2; ++half) {
+              uint32_t o[32];
+              tmem_ld32(t_o + hb * 64 + half * 32, o);
+              tmem_ld_wait();
+              reg_fence32(o);
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int ch = half * 4 + t;
+                st_shared_v4(ob + ((ch ^ (lane & 7)) << 4),
+                             pack_bf16x2(u2f(o[8 * t]) * inv_l, u2f(o[8 * t + 1]) * inv_l),
+                             pack_bf16x2(u2f(o[8 * t + 2]) * inv_l, u2f(o[8 * t + 3]) * inv_l),
+                             pack_bf16x2(u2f(o[8 * t + 4]) * inv_l, u2f(o[8 * t + 5]) * inv_l),
+                             pack_bf16x2(u2f(o[8 * t + 6]) * inv_l, u2f(o[8 * t + 7]) * inv_l));
+              }
+            }
+            if (hb == D / 64 - 1) {
+              // O_i has been read: the next unit's first P·V may overwrite it.
+              tc_fence_before_sync();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bars->o_free[wg]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && cur.r0 < p.T) {
+              tma_store_3d(&tm_o, slice, hb * 64, cur.r0, cur.bh);
+              bulk_commit_group();
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(t_o + c0, r);
+            tmem_ld_wait();
+            reg_fence32(r);
+            write_row(cur, r, c0, inv_l);
+          }
+          // O_i has been read: the next unit's first P·V may overwrite it.
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->o_free[wg]);
         }
-        // O_i has been read: the next unit's first P·V may overwrite it.
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->o_free[wg]);
         write_lse(cur, lse_of(l, m_ref));
         FA_TRACE(26 + wg, 0);
       } else {
@@ -940,7 +980,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (pend) flush_pending(false);  // the last unit's epilogue
     // The output rows' TMA stores must have read their shared-memory source before the
     // CTA exits (their global writes complete with the grid).
-    if (C::kTmaO && lane == 0) bulk_wait_group_read0();
+    if (lane == 0) bulk_wait_group_read0();
   }
 
   tc_fence_before_sync();
