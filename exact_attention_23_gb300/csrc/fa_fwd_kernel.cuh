@@ -36,6 +36,11 @@
 // Every barrier phase is counted over the CTA's whole list of units (each role walks the
 // same list and keeps the same running counts), so units follow one another with no
 // re-initialisation.
+// A unit's output leaves through shared memory: each softmax warp stages its 32 rows in
+// the O tensor map's swizzled layout and issues a TMA store. At D = 64 the epilogue is
+// deferred into the tile's first step of the next unit, after that step's P store, so that
+// the tensor core does not wait on it; at D = 128, P is stored and P·V issued in two
+// halves of the keys. (Both are described where they happen.)
 #pragma once
 
 #include "sm103.cuh"
