@@ -111,6 +111,57 @@ def test_fwd_block_sparse_parity(T, d, causal, per_head):
              f"block-sparse T{T} d{d} causal={causal} per_head={per_head}")
 
 
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+def test_fwd_block_sparse_many_units_per_cta(d, causal):
+    """B4 H12 T4096: 768 units, five or more per CTA, so each softmax warpgroup ends units
+    and starts new ones inside one launch (at d = 64 the epilogue of each is deferred into
+    the next). Per-head masks at half density, with a different empty block row in every
+    head: some units then hold a Q tile that uses no K tile at all. Heads whose CTAs differ
+    are checked in full against the oracle."""
+    import torch
+    import exact_attention_23_gb300 as fa
+    B, H, T = 4, 12, 4096
+    nb = fa.q_tiles(T)
+    q, k, v = inputs.make_qkv(B, H, T, d, 740 + d)
+    m = _mask(nb, B * H, 0.5, 741 + d)
+    for hh in range(B * H):
+        m[hh, (3 * hh) % nb, :] = 0
+    o, lse = fa.fwd_block_sparse(q.cuda(), k.cuda(), v.cuda(),
+                                 torch.from_numpy(m).cuda().contiguous(), causal=causal)
+    torch.cuda.synchronize()
+    o = o.float().cpu().double().numpy()
+    lse = lse.cpu().double().numpy()
+    for b, h in ((0, 0), (1, 5), (3, 11)):
+        o_ref, lse_ref = oracle.attention_general_head(
+            *(inputs.to_f64_numpy(t[b, h]) for t in (q, k, v)), causal, d ** -0.5, m[b * H + h])
+        _compare(o[b, h], lse[b, h], o_ref, lse_ref,
+                 f"block-sparse many units d{d} causal={causal} head ({b},{h})")
+
+
+def test_fwd_kv_prefill_many_units_per_cta_d128():
+    """B2 H12, 2048 new queries against 4096 cached keys at d = 128, bottom-right causal,
+    one key range: 192 units over the SMs, so CTAs run several in turn (P in two halves,
+    output through the staging slices). Rows sampled in three heads."""
+    import torch
+    import exact_attention_23_gb300 as fa
+    B, H, Tq, Tk, d = 2, 12, 2048, 4096, 128
+    q, k, v = _qkv_kv(B, H, Tq, Tk, d, 750)
+    o, lse = fa.fwd_kv(q.cuda(), k.cuda(), v.cuda(), causal=True, n_splits=1)
+    torch.cuda.synchronize()
+    o = o.float().cpu().double().numpy()
+    lse = lse.cpu().double().numpy()
+    rows = np.array([0, 1, 127, 128, 1023, 1024, 2047])
+    for b, h in ((0, 0), (1, 6), (1, 11)):
+        qn, kn, vn = (inputs.to_f64_numpy(t[b, h]) for t in (q, k, v))
+        # new query r is token Tk − Tq + r: it sees the keys up to and including that one
+        for r in rows:
+            o1, l1 = oracle.attention_general(qn[r:r + 1][None, None],
+                                              kn[:Tk - Tq + r + 1][None, None],
+                                              vn[:Tk - Tq + r + 1][None, None], False, d ** -0.5)
+            _compare(o[b, h, r:r + 1], lse[b, h, r:r + 1], o1[0, 0], l1[0, 0],
+                     f"kv prefill d128 head ({b},{h}) row {r}")
+
+
 def test_fwd_block_sparse_full_and_causal_masks():
     """An all-ones mask is plain attention; keeping the blocks on and below the diagonal
     under causal is plain causal attention (the skipped blocks were fully masked)."""
