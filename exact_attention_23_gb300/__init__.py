@@ -61,7 +61,9 @@ def fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=
 
     Returns (o, lse). ``out``/``lse`` may be given to reuse buffers. ``status``, an
     optional int32 CUDA tensor of one element, receives FA_ERR_TIMEOUT if an internal
-    wait of the kernel ever gives up.
+    wait of the kernel ever gives up; ``timeout_ns`` bounds those waits (0: 2 s).
+    ``flags`` is 0 except in tests of that path: FA_FLAG_TEST_STARVE_Q withholds every
+    query-tile load, FA_FLAG_TEST_STARVE_LATER_Q those after each CTA's first unit.
     """
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
