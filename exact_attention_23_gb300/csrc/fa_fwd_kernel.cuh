@@ -62,7 +62,9 @@ constexpr uint32_t kFlagStarveLaterQ = 2u;  // FA_FLAG_TEST_STARVE_LATER_Q
 template <int D, bool QK8 = false>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int kStages = (D == 64) ? 3 : 2;      // K/V ring depth (measured: 3 beats 2, 4 and 6 at d=64)
+  // K/V ring depth (measured: 3 beats 2, 4 and 6 at d=64; d = 128 in bf16 has room for 2;
+  // with e4m3 Q/K tiles half the size, 3)
+  static constexpr int kStages = (D == 64 || QK8) ? 3 : 2;
   static constexpr int kQBufs = (D == 64) ? 2 : 1;       // Q tile pairs in flight (next unit's Q)
   static constexpr int kSubBytes = kBlockM * 64 * 2;     // one 128-row × 64-col bf16 box = 16 KB
   static constexpr int kSub = D / 64;                    // boxes per tile row-block
