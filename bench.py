@@ -8,8 +8,10 @@ divided by the device time of the launches, in TFLOP/s, with the inputs already 
 in HBM. The launches of a step follow one another back to back, as a caller's would; the
 timed region has CUDA events only at its ends and around the T = 16384 launch (the roofline's
 kernel). `per_T` breaks the work down: T = 16384 from those events, the other lengths from
-back-to-back launches of one length timed after the sweep (at T ≤ 4096 their inputs then
-stay in L2). `e2e` is the same metric through the C-ABI call on host
+back-to-back launches of one length timed after the sweep, rotating over enough distinct
+input sets (≥ 640 MB together, five times the L2) that every launch reads its inputs from
+HBM. Roofline fractions divide by the measured burst bf16 peak (the kernels are timed in
+runs of milliseconds, not under a seconds-long power-capped load). `e2e` is the same metric through the C-ABI call on host
 buffers (fa_fwd_host: page-locked q, k, v in, o and lse out, the copies overlapped with the
 computation chunk by chunk), every host<->device copy inside the timed region.
 
@@ -18,7 +20,9 @@ so every launch reads inputs last touched a full step earlier.
 
 The same line carries `decode` (one query per head against a 16k-token KV cache, GB/s),
 `block_sparse` (T = 8192 with half the 128×128 blocks kept, TFLOP/s on kept blocks),
-`fp8_qk` (e4m3 queries and keys, bf16 values, B2 H16 T16384 d128, causal) and a
+`fp8_qk` (e4m3 queries and keys, bf16 values, B2 H16 T16384 d128, causal), `fwd_d128`
+(the wide-head workload B2 H16 T16384 d128, causal and non-causal), `context` (the figures
+the reference pages publish, with their hardware: context, not targets) and a
 `backward` object: the gradient pass (dQ, dK, dV through fa_bwd)
 timed the same way over the same sweep, K steps, with an upstream gradient dO drawn per T;
 FLOPs are 2.5× the forward's (five T×T×d products instead of two).
@@ -136,6 +140,8 @@ KERNEL_SOURCES = {
     "decode": ("sm103.cuh", "fa_decode_kernel.cuh", "fa_decode.cu", "fa_fwd_ext_api.cu"),
     "block_sparse": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd_gen_d64.cu", "fa_fwd_ext_api.cu"),
     "fp8": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd_fp8.cu", "fa_api.cu"),
+    "fwd_d128_causal": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd_d128.cu", "fa_api.cu"),
+    "fwd_d128_full": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd_d128.cu", "fa_api.cu"),
 }
 # The committed ncu record of each pass's dominant kernel (profiles/).
 TRAFFIC_RECORDS = {
@@ -144,6 +150,8 @@ TRAFFIC_RECORDS = {
     "decode": "dram_traffic_fa_decode_d64_b4h12_tk16384.json",
     "block_sparse": "dram_traffic_fa_fwd_block_sparse_d64_t8192.json",
     "fp8": "dram_traffic_fa_fwd_fp8_d128_causal_t16384.json",
+    "fwd_d128_causal": "dram_traffic_fa_fwd_d128_causal_b2h16_t16384.json",
+    "fwd_d128_full": "dram_traffic_fa_fwd_d128_noncausal_b2h16_t16384.json",
 }
 
 
@@ -339,6 +347,29 @@ def run_reference(args):
 DECODE_TK = 16384
 SPARSE_T = 8192
 SPARSE_DENSITY = 0.5
+# Distinct input sets rotated through when timing one length alone: together at least five
+# times the 129 MB L2, so that no launch finds its inputs in L2.
+COLD_BYTES = 640 * 2 ** 20
+
+# The figures the reference pages print for this path, with the hardware they were taken on
+# (context only: other GPUs, other code; none is a target for this metric).
+CONTEXT = {
+    "note": "figures published on the reference pages for their own kernels and hardware",
+    "figures": [
+        {"what": "best tile shape B_r x B_c", "value": "128 x 64", "hardware": "A100",
+         "source": "FlashAttention 核心思路解析 (FlashAttention core ideas), §1"},
+        {"what": "slowdown with B_r > 256 (register spills)", "value": "> 30 %",
+         "hardware": "A100", "source": "FlashAttention 核心思路解析, §1"},
+        {"what": "memory-bandwidth utilisation with aligned, conflict-free, prefetched loads",
+         "value": "65 % -> 89 %", "hardware": "A100",
+         "source": "FlashAttention 核心思路解析, §3.2"},
+        {"what": "speed-up of tiling for sequences longer than 8192", "value": "4.7x -> 11.3x",
+         "hardware": "A100 (implied)", "source": "FlashAttention 核心思路解析, §5.2"},
+        {"what": "causal forward latency, Triton 64x64 vs PyTorch SDPA vs naive, T 512-16384",
+         "value": "chart values not in the page text", "hardware": "RTX 4090",
+         "source": "手写 FlashAttention (Hand-written FlashAttention), step ⑤"},
+    ],
+}
 
 
 def _time_calls(fn, steps, warmup, stream, torch, ws):
@@ -357,7 +388,7 @@ def _time_calls(fn, steps, warmup, stream, torch, ws):
     return _max_over_ranks(a.elapsed_time(b), ws) / steps
 
 
-def _bwd_d128(args, fa, inputs, torch, dev, stream, bf16_sus, ws):
+def _bwd_d128(args, fa, inputs, torch, dev, stream, bf16_peak, ws):
     """Backward at head dim 128 on the wide-head workload (B2 H16 T16384, causal)."""
     Bw, Hw, Tw, Dw = 2, 16, 16384, 128
     q, k, v = (t.to(dev) for t in inputs.make_qkv(Bw, Hw, Tw, Dw, seed=10))
@@ -378,14 +409,14 @@ def _bwd_d128(args, fa, inputs, torch, dev, stream, bf16_sus, ws):
     tf = ws * fa.bwd_flops(Bw, Hw, Tw, Dw, True) / ms / 1e9
     return {"workload": "causal attention backward, bf16, B2 H16 T16384 d128", "value": tf,
             "unit": "TFLOP/s", "ms_per_call": ms, "steps": steps,
-            "frac_of_sustained": tf / ws / bf16_sus, "gpu_launches": 3 * steps}
+            "frac_of_burst": tf / ws / bf16_peak, "gpu_launches": 3 * steps}
 
 
-def _fwd_fp8(args, fa, inputs, torch, dev, stream, bf16_sus, ws):
+def _fwd_fp8(args, fa, inputs, torch, dev, stream, bf16_peak, ws):
     """Forward with e4m3 Q/K codes (per-tensor scales) and bf16 V on the wide-head workload
     (B2 H16 T16384 d128, causal), with the bf16 forward on the same values beside it. Q·Kᵀ
     runs on the 8-bit tensor path (nominally 2x bf16) and P·V on the bf16 one, so the peak
-    for the mix is 2/(1/(2·P) + 1/P) = 4/3·P for the sustained bf16 peak P."""
+    for the mix is 2/(1/(2·P) + 1/P) = 4/3·P for the measured burst bf16 peak P."""
     Bw, Hw, Tw, Dw = 2, 16, 16384, 128
     q8, sq, k8, sk, v = inputs.make_qk_fp8(Bw, Hw, Tw, Dw, seed=30)
     q8, k8, v = q8.to(dev), k8.to(dev), v.to(dev)
@@ -411,7 +442,7 @@ def _fwd_fp8(args, fa, inputs, torch, dev, stream, bf16_sus, ws):
     ms8 = _time_calls(call8, steps, args.warmup, stream, torch, ws)
     ms16 = _time_calls(call16, steps, args.warmup, stream, torch, ws)
     tf8, tf16 = ws * fl / ms8 / 1e9, ws * fl / ms16 / 1e9
-    peak = 4.0 / 3.0 * bf16_sus
+    peak = 4.0 / 3.0 * bf16_peak
     return {"workload": "causal attention forward, e4m3 Q/K (per-tensor scales), bf16 V, "
                         "B2 H16 T16384 d128",
             "value": tf8, "unit": "TFLOP/s", "ms_per_call": ms8, "steps": steps,
@@ -419,12 +450,44 @@ def _fwd_fp8(args, fa, inputs, torch, dev, stream, bf16_sus, ws):
             "roofline": {"bound": "tensor", "achieved": tf8 / ws, "peak": peak,
                          "unit": "TFLOP/s", "frac": tf8 / ws / peak,
                          "traffic": _measured_traffic("fp8"),
-                         "peak_basis": "4/3 x sustained bf16 of measured (Q·Kᵀ at the "
+                         "peak_basis": "4/3 x burst bf16 of measured (Q·Kᵀ at the "
                                        "nominal 2x 8-bit rate, P·V at bf16)"},
             "gpu_launches": 2 * steps}
 
 
-def _general_forms(args, fa, inputs, torch, dev, stream, bf16_sus, hbm_peak, ws):
+def _fwd_d128(args, fa, inputs, torch, dev, stream, bf16_peak, ws):
+    """The wide-head long-context workload (B2 H16 T16384 d128, q/k/v bf16 N(0,1) drawn with
+    seed 10), causal and non-causal: K calls each (<= 20), with a roofline against the burst
+    bf16 peak and the committed DRAM-traffic record of each launch."""
+    Bw, Hw, Tw, Dw = 2, 16, 16384, 128
+    q, k, v = (t.to(dev) for t in inputs.make_qkv(Bw, Hw, Tw, Dw, seed=10))
+    o = torch.empty_like(q)
+    lse = torch.empty((Bw, Hw, Tw), dtype=torch.float32, device=dev)
+    steps = max(1, min(args.steps, 20))
+    out = {"workload": "attention forward, bf16, B2 H16 T16384 d128 (wide head, long context)"}
+    for causal, key in ((1, "causal"), (0, "non_causal")):
+        def call():
+            rc = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           Bw, Hw, Tw, Dw, causal, Dw ** -0.5, stream.cuda_stream)
+            if rc != fa.FA_OK:
+                raise fa.FAError(rc, "fa_fwd")
+        ms = _time_calls(call, steps, args.warmup, stream, torch, ws)
+        fl = fa.flops(Bw, Hw, Tw, Dw, bool(causal))
+        tf = ws * fl / ms / 1e9
+        out[key] = {
+            "value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "steps": steps,
+            "roofline": {"bound": "tensor", "achieved": tf / ws, "peak": bf16_peak,
+                         "unit": "TFLOP/s", "frac": tf / ws / bf16_peak,
+                         "traffic": _measured_traffic("fwd_d128_causal" if causal else "fwd_d128_full"),
+                         "algorithmic_bytes": fa.hbm_bytes(Bw, Hw, Tw, Dw),
+                         "kernel": f"fa_fwd_kernel<128,{'causal' if causal else 'non-causal'}>; "
+                                   f"{fl:.4g} FLOP per launch; peak = burst bf16"},
+            "gpu_launches": steps,
+        }
+    return out
+
+
+def _general_forms(args, fa, inputs, torch, dev, stream, bf16_peak, hbm_peak, ws):
     """Decode (one new query per head against a 16k-token KV cache, B4 H12 d64, key range
     split over CTAs) and block-sparse self-attention (T = 8192, half of the 128×128 blocks
     kept at random, non-causal). Inputs are allocated before timing; K steps each."""
@@ -484,8 +547,8 @@ def _general_forms(args, fa, inputs, torch, dev, stream, bf16_sus, hbm_peak, ws)
                   "50% random 128x128 blocks, non-causal)",
         "value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "kept_blocks": kept,
         "blocks": nb * nb, "steps": args.steps,
-        "roofline": {"bound": "tensor", "achieved": tf / ws, "peak": bf16_sus, "unit": "TFLOP/s",
-                     "frac": tf / ws / bf16_sus, "traffic": _measured_traffic("block_sparse"),
+        "roofline": {"bound": "tensor", "achieved": tf / ws, "peak": bf16_peak, "unit": "TFLOP/s",
+                     "frac": tf / ws / bf16_peak, "traffic": _measured_traffic("block_sparse"),
                      "kernel": "fa_fwd_kernel<64,non-causal,general> with a block mask; FLOPs "
                                "= 4·B·H·128²·d per kept block"},
         "gpu_launches": args.steps,
@@ -514,22 +577,44 @@ def _time_sweep(torch, stream, items, launch, steps, dom):
     return t_start, t_end, ev
 
 
-def _time_each(torch, stream, items, launch, steps, skip):
-    """Mean ms per launch of every item but `skip`, timed apart from the sweep: `steps`
-    back-to-back launches of that item between two events."""
-    out = {}
-    for j, item in enumerate(items):
-        if j == skip:
-            continue
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(steps):
-            launch(item)
-        b.record(stream)
-        torch.cuda.synchronize()
-        out[j] = a.elapsed_time(b) / steps
-    return out
+def _n_cold_sets(set_bytes: float) -> int:
+    """Distinct input sets that together reach COLD_BYTES."""
+    return max(1, -(-int(COLD_BYTES) // max(1, int(set_bytes))))
+
+
+def _time_rotating(torch, stream, sets, launch, steps):
+    """Mean ms per launch over back-to-back launches that rotate through `sets` (each used
+    at least twice, at least `steps` launches in all), between two events on the stream."""
+    n = len(sets)
+    reps = max(2, -(-steps // n))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    for s_ in sets:  # warm: code, tensor-map descriptors, first-touch of every buffer
+        launch(s_)
+    a.record(stream)
+    for _ in range(reps):
+        for s_ in sets:
+            launch(s_)
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (reps * n), n
+
+
+def run_only(args):
+    """One object of the line alone: with --warmup W and --steps K its launches run in a
+    fixed order (for fwd_d128: W + K causal, then W + K non-causal), so a profiler can pick
+    one by its index."""
+    import torch
+
+    import exact_attention_23_gb300 as fa
+    from exact_attention_23_gb300 import inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    bf16_peak, _, _, _ = _peaks()
+    out = _fwd_d128(args, fa, inputs, torch, dev, stream, bf16_peak, 1)
+    print(json.dumps({"only": args.only, **out}), flush=True)
+    return 0
 
 
 def run_gpu(args):
@@ -583,7 +668,19 @@ def run_gpu(args):
     value, elapsed_ms = aggregate_tflops(flops_step, args.steps, t_start.elapsed_time(t_end), ws)
     launches = args.steps * len(sets)
     dom_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    others = _time_each(torch, stream, sets, launch, args.steps, jdom)
+    others, n_sets = {}, {}
+    for j, s_ in enumerate(sets):
+        if j == jdom:
+            continue
+        T = s_[0]
+        cold = []
+        for _ in range(_n_cold_sets(fa.hbm_bytes(B, H, T, D))):
+            qc, kc, vc = (torch.randn((B, H, T, D), device=dev, dtype=torch.bfloat16)
+                          for _ in range(3))
+            cold.append((T, None, None, None, qc, kc, vc, torch.empty_like(qc),
+                         torch.empty((B, H, T), dtype=torch.float32, device=dev)))
+        others[j], n_sets[j] = _time_rotating(torch, stream, cold, launch, args.steps)
+        del cold
 
     bf16_peak, bf16_sus, hbm_peak, peak_kind = _peaks()
     per_T = []
@@ -593,8 +690,9 @@ def run_gpu(args):
         fl = fa.flops(B, H, T, D, True)
         by = fa.hbm_bytes(B, H, T, D)
         per_T.append({"T": T, "ms": ms, "tflops": fl / ms / 1e9,
-                      "frac_of_sustained": fl / ms / 1e9 / bf16_sus,
-                      "gbs": by / ms / 1e6, "frac_hbm": by / ms / 1e6 / hbm_peak})
+                      "frac_of_burst": fl / ms / 1e9 / bf16_peak,
+                      "gbs": by / ms / 1e6, "frac_hbm": by / ms / 1e6 / hbm_peak,
+                      "input_sets": 1 if j == jdom else n_sets[j]})
     dom = max(per_T, key=lambda r: fa.flops(B, H, r["T"], D, True))
 
     # ---- backward: the same sweep, K steps, dO drawn per T, workspace allocated up front
@@ -630,23 +728,41 @@ def run_gpu(args):
     bflops_step = sum(fa.bwd_flops(B, H, T, D, True) for T in sweep)
     bvalue, b_ms = aggregate_tflops(bflops_step, args.steps, b_start.elapsed_time(b_end), ws)
     bdom_ms = statistics.mean(a.elapsed_time(b) for a, b in bev)
-    bothers = _time_each(torch, stream, bsets, launch_bwd, args.steps, jdom)
+    del bsets
+    bothers, bn_sets = {}, {}
+    for j, s_ in enumerate(sets):
+        if j == jdom:
+            continue
+        T = s_[0]
+        ws_t = fa.bwd_workspace(B, H, T, D, device=dev)  # scratch only: shared by the sets
+        # q, k, v, o, dO, dQ, dK, dV (bf16) and lse: a set's bytes
+        cold = []
+        for _ in range(_n_cold_sets(B * H * T * (8.0 * D * 2 + 4.0))):
+            qc, kc, vc, doc = (torch.randn((B, H, T, D), device=dev, dtype=torch.bfloat16)
+                               for _ in range(4))
+            oc, lc = fa.fwd(qc, kc, vc, causal=True)
+            cold.append((T, qc, kc, vc, oc, lc, doc, tuple(torch.empty_like(qc) for _ in range(3)),
+                         ws_t))
+        bothers[j], bn_sets[j] = _time_rotating(torch, stream, cold, launch_bwd, args.steps)
+        del cold, ws_t
     bper_T = []
-    for j, bs in enumerate(bsets):
-        T = bs[0]
+    for j, s_ in enumerate(sets):
+        T = s_[0]
         ms = bdom_ms if j == jdom else bothers[j]
         fl = fa.bwd_flops(B, H, T, D, True)
         bper_T.append({"T": T, "ms": ms, "tflops": fl / ms / 1e9,
-                       "frac_of_sustained": fl / ms / 1e9 / bf16_sus})
+                       "frac_of_burst": fl / ms / 1e9 / bf16_peak,
+                       "input_sets": 1 if j == jdom else bn_sets[j]})
     bdom = max(bper_T, key=lambda r: r["T"])
-    del bsets
     # head dim 128 (64-query tiles): the wide-head workload, B2 H16 T16384
-    b128 = _bwd_d128(args, fa, inputs, torch, dev, stream, bf16_sus, ws)
+    b128 = _bwd_d128(args, fa, inputs, torch, dev, stream, bf16_peak, ws)
 
     # ---- general forms: decode against a KV cache (split key ranges), block-sparse
-    extra = _general_forms(args, fa, inputs, torch, dev, stream, bf16_sus, hbm_peak, ws)
+    extra = _general_forms(args, fa, inputs, torch, dev, stream, bf16_peak, hbm_peak, ws)
     # ---- FP8 (e4m3) queries and keys at head dim 128
-    extra["fp8_qk"] = _fwd_fp8(args, fa, inputs, torch, dev, stream, bf16_sus, ws)
+    extra["fp8_qk"] = _fwd_fp8(args, fa, inputs, torch, dev, stream, bf16_peak, ws)
+    # ---- the wide-head workload's forward, causal and non-causal
+    extra["fwd_d128"] = _fwd_d128(args, fa, inputs, torch, dev, stream, bf16_peak, ws)
 
     # ---- end to end: the C-ABI call on host buffers (fa_fwd_host: page-locked q, k, v in,
     # o, lse out; chunks of heads copied in, attended and copied back on overlapping
@@ -707,37 +823,42 @@ def run_gpu(args):
                        "B": B, "H": H, "d": D, "T": sweep, "causal": True,
                        "parallelism": f"replicas{ws}" if ws > 1 else "single GPU",
                        "l2": "inputs larger than L2: ~0.8 GB of distinct tensors per step" if not args.T else "single T"},
-            "frac_of_peak": {"sustained": value / ws / bf16_sus, "burst": value / ws / bf16_peak,
+            "frac_of_peak": {"burst": value / ws / bf16_peak, "sustained": value / ws / bf16_sus,
                              "peak_kind": peak_kind},
             "per_T": per_T,
-            "per_T_note": ("T=16384 timed inside the sweep; the other lengths as back-to-back "
-                           "launches of one length after it"),
-            "roofline": {"bound": "tensor", "achieved": dom["tflops"], "peak": bf16_sus,
-                         "unit": "TFLOP/s", "frac": dom["tflops"] / bf16_sus,
+            "per_T_note": ("T=16384 timed inside the sweep; each other length alone, "
+                           "back-to-back launches rotating over input_sets distinct input sets "
+                           f"(>= {COLD_BYTES >> 20} MB together, > 4x L2), so inputs come from "
+                           "HBM; frac_of_burst against the measured burst bf16 peak, frac_hbm "
+                           "against the measured HBM copy rate"),
+            "roofline": {"bound": "tensor", "achieved": dom["tflops"], "peak": bf16_peak,
+                         "unit": "TFLOP/s", "frac": dom["tflops"] / bf16_peak,
                          "traffic": args.traffic if args.traffic is not None else (
                              _measured_traffic() if dom["T"] == 16384 else None),
                          "algorithmic_bytes": fa.hbm_bytes(B, H, dom["T"], D),
                          "kernel": f"fa_fwd_kernel<64,causal> at T={dom['T']} "
                                    f"({fa.flops(B, H, dom['T'], D, True):.4g} FLOP per launch; "
-                                   f"peak = {peak_kind} sustained bf16)"},
+                                   f"peak = {peak_kind} burst bf16)"},
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
             "gpu_launches": launches,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "context": CONTEXT,
             **extra,
             "backward": {
                 "metric": BWD_METRIC, "value": bvalue, "unit": "TFLOP/s",
                 "ms_per_step": b_ms / args.steps, "steps": args.steps,
-                "frac_of_peak": {"sustained": bvalue / ws / bf16_sus, "peak_kind": peak_kind},
+                "frac_of_peak": {"burst": bvalue / ws / bf16_peak,
+                                 "sustained": bvalue / ws / bf16_sus, "peak_kind": peak_kind},
                 "per_T": bper_T,
-                "roofline": {"bound": "tensor", "achieved": bdom["tflops"], "peak": bf16_sus,
-                             "unit": "TFLOP/s", "frac": bdom["tflops"] / bf16_sus,
+                "roofline": {"bound": "tensor", "achieved": bdom["tflops"], "peak": bf16_peak,
+                             "unit": "TFLOP/s", "frac": bdom["tflops"] / bf16_peak,
                              "traffic": _measured_traffic("bwd") if bdom["T"] == 16384 else None,
                              "kernel": f"fa_bwd_main_kernel<64,causal> at T={bdom['T']}; achieved "
                                        f"over the whole fa_bwd call (prep + main + dQ conversion), "
                                        f"{fa.bwd_flops(B, H, bdom['T'], D, True):.4g} FLOP; peak = "
-                                       f"{peak_kind} sustained bf16"},
+                                       f"{peak_kind} burst bf16"},
                 "gpu_launches": 3 * args.steps * len(sweep),
                 "d128": b128,
                 "clocks": bclocks,
@@ -760,6 +881,8 @@ def main():
     ap.add_argument("--T", type=int, default=0, help="time one length instead of the sweep")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=("fwd_d128",), default=None,
+                    help="run one object alone (for a profiler capture) and print it")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()
@@ -767,6 +890,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.only:
+        return run_only(args)
     return run_gpu(args)
 
 

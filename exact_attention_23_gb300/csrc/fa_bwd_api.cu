@@ -36,7 +36,7 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
     return FA_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || T <= 0 || (d != 64 && d != 128)) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   if ((flags & ~static_cast<unsigned>(FA_FLAG_TEST_STARVE_Q)) != 0u) return FA_ERR_INVALID_ARG;
   const size_t need = fa_bwd_workspace_size(B, H, T, d);
   if (need == 0 || workspace_bytes < need) return FA_ERR_INVALID_ARG;

@@ -116,7 +116,6 @@ struct BwdBars {
   uint64_t grad_done;   // every MMA of the gradient issuer done: dK, dV final
   uint32_t tmem_base;
   uint32_t abort;
-  uint32_t never;       // stays 0: abort flag of the teardown waits, which must not be cut short
 };
 static_assert(sizeof(BwdBars) <= 256, "barrier block");
 
@@ -345,7 +344,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(&bars->score_done, 1);
     mbar_init(&bars->grad_done, 1);
     bars->abort = 0u;
-    bars->never = 0u;
     fence_mbar_init();
   }
   if (warp == C::kScoreWarp) {
@@ -362,7 +360,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   pdl_wait();
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort, p.status, p.timeout_ns};
-  const WaitCtl drain_wc{&bars->never, nullptr, p.timeout_ns};
+  const WaitCtl drain_wc = drain_ctl(p.timeout_ns);
   const uint32_t sbase = smem_u32(sm);
   auto q_s = [&](int st) { return sbase + C::kStage0 + st * C::kStageBytes; };
   auto do_s = [&](int st) { return q_s(st) + C::kQTile; };

@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kDecBlock, kDecCtasPerSm)
   constexpr int kWarps = kDecThreads / 32;     // compute warps; warp kWarps is the producer
   extern __shared__ __align__(128) uint8_t ring[];  // stage s: K chunk, then V chunk
   __shared__ uint64_t full[kDecStages], empty[kDecStages];
-  __shared__ uint32_t abort_flag, never;
+  __shared__ uint32_t abort_flag;
   __shared__ float wm[kWarps], wl[kWarps];
   __shared__ __align__(16) float wo[kWarps][D];
   // Launched as a programmatic dependent: the previous kernel on the stream (possibly the
@@ -90,7 +90,6 @@ __global__ void __launch_bounds__(kDecBlock, kDecCtasPerSm)
       mbar_init(&empty[s], kWarps);
     }
     abort_flag = 0u;
-    never = 0u;
     fence_mbar_init();
   }
   __syncthreads();
@@ -116,7 +115,7 @@ __global__ void __launch_bounds__(kDecBlock, kDecCtasPerSm)
     }
     // Every copy issued must have landed before the CTA may exit (the compute warps have
     // consumed them all unless a wait gave up).
-    const WaitCtl drain{&never, nullptr, 2000000000ull};
+    const WaitCtl drain = drain_ctl(0);
     for (int x = c > kDecStages ? c - kDecStages : 0; x < c; ++x)
       mbar_wait_warp(&full[x % kDecStages], (x / kDecStages) & 1, drain);
   } else {

@@ -106,7 +106,8 @@ int launch_general(const GenArgs& g, int sms) {
   a.p.n_kv = static_cast<int>(n_kt);
   a.p.tiles_per_cta = tiles;
   a.p.div_bh = fa::FastDiv::make(static_cast<uint32_t>(BH));
-  a.p.scale_log2 = static_cast<float>(static_cast<double>(g.scale) * 1.4426950408889634074);
+  a.p.scale_log2 = exponent_factor(static_cast<double>(g.scale) * 1.4426950408889634074,
+                                   &a.p.s_negate);
   a.p.timeout_ns = g.timeout_ns ? g.timeout_ns : 2000000000ull;
   a.p.flags = 0u;
   a.p.Tk = g.Tk;
@@ -139,7 +140,7 @@ int validate_common(const void* q, const void* k, const void* v, const void* o, 
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || Tq <= 0 || Tk <= 0) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > INT32_MAX) return FA_ERR_INVALID_ARG;
   const long long Tmax = std::max(Tq, Tk);

@@ -65,6 +65,7 @@ struct Cfg {
   // K/V ring depth (measured: 3 beats 2, 4 and 6 at d=64; d = 128 in bf16 has room for 2;
   // with e4m3 Q/K tiles half the size, 3)
   static constexpr int kStages = (D == 64 || QK8) ? 3 : 2;
+  static_assert(kStages >= 1 && kStages <= 4, "K/V ring depth (barrier arrays hold 4)");
   static constexpr int kQBufs = (D == 64) ? 2 : 1;       // Q tile pairs in flight (next unit's Q)
   static constexpr int kSubBytes = kBlockM * 64 * 2;     // one 128-row × 64-col bf16 box = 16 KB
   static constexpr int kSub = D / 64;                    // boxes per tile row-block
@@ -120,7 +121,6 @@ struct Bars {
   uint64_t mma_done;
   uint32_t tmem_base;
   uint32_t abort;
-  uint32_t never;  // stays 0: abort flag of the drain waits, which must not be cut short
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
@@ -152,7 +152,9 @@ struct FwdParams {
   int tiles_per_cta;  // 2 (ping-pong pair) or 1 (short sequences: more CTAs)
   FastDiv div_bh;     // division by BH
   FastDiv div_splits; // division by n_splits (general form)
-  float scale_log2;   // scale · log2(e)
+  float scale_log2;   // |scale| · log2(e) (the smallest normal float when scale = 0)
+  uint32_t s_negate;  // kIdescNegateA when scale < 0 (S = −Q·Kᵀ, so that S·scale_log2 keeps its
+                      // sign), else 0
   uint64_t timeout_ns;
   uint32_t flags;
   // General form only (GEN kernels; T above is then the query length Tq):
@@ -310,7 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars->mma_done, 2);
     bars->abort = 0u;
-    bars->never = 0u;
     fence_mbar_init();
   }
   if (warp == 8) {
@@ -326,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_launch_dependents();
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort, p.status, p.timeout_ns};
-  const WaitCtl drain{&bars->never, nullptr, p.timeout_ns};
+  const WaitCtl drain = drain_ctl(p.timeout_ns);
 
   if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
@@ -409,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 8) {
       // S_i = Q_i · K_stᵀ : M=128, N=128, K=D in steps of 16 (32 bytes inside a 128-byte
       // swizzled row; a new 16 KB box every 64 columns). Committed to s_full[i].
-      constexpr uint32_t kIdescS = idesc_bf16(kBlockM, kBlockN, false);
+      const uint32_t kIdescS = idesc_bf16(kBlockM, kBlockN, false) | p.s_negate;
       const uint32_t q_base = smem_u32(smem + C::kQOff);
       const uint32_t k_base = smem_u32(smem + C::kKOff);
       auto issue_s = [&](int qb, int i, int st) {
@@ -418,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ka = k_base + st * C::kQKTileBytes;
           if constexpr (QK8) {
             // e4m3: K = 32 codes = 32 bytes per instruction inside one swizzled row
-            constexpr uint32_t kIdescS8 = idesc_e4m3(kBlockM, kBlockN);
+            const uint32_t kIdescS8 = idesc_e4m3(kBlockM, kBlockN) | p.s_negate;
 #pragma unroll
             for (int kk = 0; kk < D / 32; ++kk) {
               const uint32_t off = kk * 32;

@@ -22,6 +22,15 @@ int check_device(int* dev_out, int* sms_out);
 bool encode_map(EncodeTiledFn enc, CUtensorMap* map, const void* base, int T, int d, int BH,
                 int box_rows = 128);
 bool overlaps(const void* a, size_t na, const void* b, size_t nb);
+// A softmax factor the kernels can take: finite, and so is scale·log2(e) in fp32 (every
+// sign and zero included).
+bool scale_ok(float scale);
+// The tensor-core kernels' exponent factor for scale·log2(e) = sl2: they take the row
+// maximum of S before multiplying by the factor, so the factor must be positive. sl2 < 0
+// runs as S = −Q·Kᵀ (the S product's A-negate bit, *negate) with factor −sl2; sl2 = 0 runs
+// with the smallest normal float, under which every score s with |s| < 2^102 gives
+// exactly 2^(s·c − m) = 1 (uniform weights) and masked scores still give 0.
+float exponent_factor(double sl2, unsigned* negate);
 bool aligned16(const void* p);
 
 }  // namespace host

@@ -107,7 +107,7 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
   // ---- host-side validation: nothing is enqueued on failure
   if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
   if (!sizes_ok(B, H, T, d) || heads_per_chunk < 0) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || !(scale > 0.0f)) return FA_ERR_INVALID_ARG;
+  if (!fa::host::scale_ok(scale)) return FA_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return FA_ERR_MISALIGNED;
   const long long BH = static_cast<long long>(B) * H;
   const size_t tbytes = static_cast<size_t>(BH * T * d * 2);

@@ -45,6 +45,9 @@ cudaError_t launch_fwd_d64(const FwdLaunch& a, bool causal);
 cudaError_t launch_fwd_d128(const FwdLaunch& a, bool causal);
 // Q and K as e4m3 codes (tensor maps over bytes), d ∈ {64, 128}.
 cudaError_t launch_fwd_fp8(const FwdLaunch& a, int d, bool causal);
+// One 128-row Q tile per CTA with double-buffered S and P (fa_fwd1_kernel.cuh); a.p holds one
+// tile per unit (tiles_per_cta = 1), d ∈ {64, 128}.
+cudaError_t launch_fwd1(const FwdLaunch& a, int d, bool causal);
 
 // General form (Tq ≠ Tk, bottom-right causal, block masks, key ranges): the forward kernel
 // with GEN = true, then, when a.p.n_splits > 1, the merge of the partial results.

@@ -69,12 +69,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // What a bounded wait needs to know: the CTA's abort flag (shared memory), the
 // optional device status word and the limit.
 struct WaitCtl {
-  volatile uint32_t* abort;  // shared-memory flag; nonzero once any role gave up
+  volatile uint32_t* abort;  // shared-memory flag; nonzero once any role gave up. Null for
+                             // a drain wait: it is neither cut short by another role's
+                             // failure nor does its own time-out mark the CTA as failed.
   int* status;               // optional global status word (may be null)
   uint64_t timeout_ns;
 };
 
 constexpr int kErrTimeout = 5;  // equals FA_ERR_TIMEOUT in fa.h
+
+// The wait of a teardown step (copies or MMAs still in flight before the CTA exits or frees
+// tensor memory): independent of the abort flag, and never shorter than two seconds,
+// whatever limit the caller chose for the ordinary waits.
+constexpr uint64_t kDrainMinNs = 2000000000ull;
+__host__ __device__ __forceinline__ WaitCtl drain_ctl(uint64_t timeout_ns) {
+  return WaitCtl{nullptr, nullptr, timeout_ns > kDrainMinNs ? timeout_ns : kDrainMinNs};
+}
 
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, WaitCtl w) {
   // try_wait itself suspends the thread for a short while, so plain polling costs no
@@ -85,9 +95,9 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0u) {
-      if (*w.abort) return false;
+      if (w.abort && *w.abort) return false;
       if (global_timer_ns() - t0 > w.timeout_ns) {
-        *w.abort = 1u;
+        if (w.abort) *w.abort = 1u;
         if (w.status) atomicExch(w.status, kErrTimeout);
         return false;
       }
@@ -116,12 +126,12 @@ static __device__ __noinline__ bool mbar_wait_warp_slow(uint64_t* bar, uint32_t 
     if ((it & 63u) == 0u) {
       uint32_t verdict = 0u;  // 1 = give up (another role aborted), 2 = timed out here
       if ((threadIdx.x & 31u) == 0u) {
-        if (*w.abort) verdict = 1u;
+        if (w.abort && *w.abort) verdict = 1u;
         else if (global_timer_ns() - t0 > w.timeout_ns) verdict = 2u;
       }
       verdict = __shfl_sync(0xffffffffu, verdict, 0);
       if (verdict == 2u && (threadIdx.x & 31u) == 0u) {
-        *w.abort = 1u;
+        if (w.abort) *w.abort = 1u;
         if (w.status) atomicExch(w.status, kErrTimeout);
       }
       if (verdict != 0u) return false;
@@ -149,12 +159,12 @@ __device__ __forceinline__ bool mbar_wait_warp_inl(uint64_t* bar, uint32_t parit
     if ((it & 63u) == 0u) {
       uint32_t verdict = 0u;  // 1 = give up (another role aborted), 2 = timed out here
       if ((threadIdx.x & 31u) == 0u) {
-        if (*w.abort) verdict = 1u;
+        if (w.abort && *w.abort) verdict = 1u;
         else if (global_timer_ns() - t0 > w.timeout_ns) verdict = 2u;
       }
       verdict = __shfl_sync(0xffffffffu, verdict, 0);
       if (verdict == 2u && (threadIdx.x & 31u) == 0u) {
-        *w.abort = 1u;
+        if (w.abort) *w.abort = 1u;
         if (w.status) atomicExch(w.status, kErrTimeout);
       }
       if (verdict != 0u) return false;
@@ -331,6 +341,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, bool b
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          ((N >> 3) << 17) | ((M >> 4) << 24);
 }
+
+// Bit 13 of a kind::f16 / kind::f8f6f4 instruction descriptor: the product is taken with A
+// negated (D (+)= (−A)·B), exactly, since negation only flips sign bits.
+constexpr uint32_t kIdescNegateA = 1u << 13;
 
 // Same with both operand majors explicit (A MN-major sets bit 15).
 __host__ __device__ constexpr uint32_t idesc_bf16_ab(uint32_t M, uint32_t N, bool a_mn_major,

@@ -65,7 +65,8 @@ typedef enum {
  *   lse     : float*, [B, H, T], device memory, written (natural-log logsumexp of the
  *             scaled scores of each query row)
  *   causal  : nonzero → key j is visible to query i only when j ≤ i
- *   scale   : multiplies Q Kᵀ (1/√d for standard attention); must be finite and > 0
+ *   scale   : multiplies Q Kᵀ (1/√d for standard attention); any finite value: 0 weighs
+ *             every visible key equally, a negative value favours the lowest scores
  *   stream  : cudaStream_t or NULL
  *
  * Returns FA_OK or an fa_status code; see the conventions above.
@@ -227,7 +228,9 @@ int fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const 
  *     B·H·ceil(T/128)·128·66·4 bytes > 32 MiB, e.g. B·H = 12 allows T ≤ 10496.
  *   - The first call on each device looks up the reservation's device address (which
  *     may load the library's device code); FA_ERR_LAUNCH if that fails. Make that first
- *     call before any stream capture on the device.
+ *     call before any stream capture on the device. The address is kept per device
+ *     together with the id of the context it was found in; after a device reset (a new
+ *     context) the next call looks it up again, so make that call before any capture too.
  *   - There is one reservation per device: calls that may overlap in time on the same
  *     device (different streams, or several host threads) race on it and give wrong
  *     results. Order them on one stream, or with events.

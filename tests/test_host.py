@@ -83,8 +83,13 @@ def _call(q=A, k=A + SZ, v=A + 2 * SZ, o=A + 3 * SZ, lse=A + 4 * SZ, B=1, H=1, T
     (dict(d=256), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
-    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
-    (dict(scale=-0.125), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("-inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=3.0e38), fa.FA_ERR_INVALID_ARG),        # scale·log2(e) overflows fp32
+    # every finite scale passes validation (0: uniform weights; < 0: reversed preference):
+    # these fail only at the misaligned pointer, checked later, before any device call
+    (dict(scale=0.0, q=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(scale=-0.125, q=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(scale=-1.0e30, q=A + 8), fa.FA_ERR_MISALIGNED),
     (dict(flags=4), fa.FA_ERR_INVALID_ARG),
     (dict(q=A + 8), fa.FA_ERR_MISALIGNED),
     (dict(o=A + 3 * SZ + 2), fa.FA_ERR_MISALIGNED),

@@ -76,6 +76,76 @@ def test_parity_ragged_lengths(T, d, causal):
     _full_check(w, rounding_allowance=True)
 
 
+@pytest.mark.parametrize("T", [1100, 1281])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_parity_odd_tile_count_in_pairs(T, d, causal):
+    """An odd number of 128-row query tiles while the kernel runs two tiles per work unit:
+    the last unit of every head holds one tile, the producer still issues the pair's
+    second (wholly out-of-range) query box and one softmax warpgroup sits that unit out.
+    B4 H12 gives enough units that the host picks pairs (pairs at least fill the SMs)."""
+    torch = _torch()
+    B, H = 4, 12
+    n_qt = -(-T // 128)
+    assert n_qt % 2 == 1
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ((n_qt + 1) // 2) * B * H >= sms, "the host would pick single-tile units"
+    w = inputs.Workload(f"odd_tiles_t{T}_d{d}", B, H, T, d, causal, 2000 + T + d)
+    _full_check(w)
+
+
+@pytest.mark.parametrize("T", [1153, 1409])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_parity_ragged_in_pairs(T, d, causal):
+    """Ragged last tiles (T not a multiple of 128) on the two-tile-per-CTA kernel: B4 H12 has
+    enough pairs to fill the SMs, so the host runs pairs rather than single tiles."""
+    torch = _torch()
+    B, H = 4, 12
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ((-(-T // 128) + 1) // 2) * B * H >= sms, "the host would pick single-tile units"
+    _full_check(inputs.Workload(f"pairs_t{T}_d{d}", B, H, T, d, causal, 2500 + T + d))
+
+
+@pytest.mark.parametrize("scale", [-0.125, -0.05])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_parity_negative_scale(scale, d, causal):
+    """A negative factor on QKᵀ (the step S = QKᵀ/√d takes the factor from the caller): the
+    row maximum of the scaled scores comes from the smallest raw score, and masked scores
+    must still weigh nothing. Ragged T = 777 (a partial last tile)."""
+    q, k, v = inputs.make_qkv(1, 3, 777, d, seed=3000 + d)
+    o, lse = _run(q, k, v, causal, scale=scale)
+    o_ref, lse_ref = oracle.attention(inputs.to_f64_numpy(q), inputs.to_f64_numpy(k),
+                                      inputs.to_f64_numpy(v), causal, scale)
+    _compare(o, lse, o_ref, lse_ref, f"scale {scale} d{d} causal={causal}",
+             rounding_allowance=True)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_scale_zero_is_uniform_attention(d, causal):
+    """scale = 0: every visible key weighs the same, whatever q and k hold. O_i is the mean
+    of the visible v rows and LSE_i = ln(visible count): the closed form, and the oracle
+    agrees. T = 333 (ragged)."""
+    T = 333
+    q, k, v = inputs.make_qkv(1, 2, T, d, seed=3100 + d)
+    o, lse = _run(q, k, v, causal, scale=0.0)
+    vv = inputs.to_f64_numpy(v)
+    if causal:
+        want_o = np.cumsum(vv, axis=2) / np.arange(1, T + 1)[None, None, :, None]
+        want_l = np.log(np.arange(1, T + 1))[None, None]
+    else:
+        want_o = np.broadcast_to(vv.mean(axis=2, keepdims=True), vv.shape)
+        want_l = np.full((1, 2, T), math.log(T))
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    assert np.max(np.abs(o - want_o)) <= O_MAX
+    assert np.max(np.abs(lse - want_l)) <= LSE_MAX
+    o_ref, lse_ref = oracle.attention(inputs.to_f64_numpy(q), inputs.to_f64_numpy(k), vv, causal,
+                                      0.0)
+    _compare(o, lse, o_ref, lse_ref, f"scale 0 d{d} causal={causal}", rounding_allowance=True)
+
+
 def _sample_rows(T, rng, n_random=48):
     fixed = [0, 1, 2, 127, 128, 129, 255, 256, T // 2, T - 129, T - 128, T - 2, T - 1]
     rows = set(r for r in fixed if 0 <= r < T)

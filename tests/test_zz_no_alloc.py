@@ -21,12 +21,18 @@ def test_noalloc_rejects_sizes_beyond_the_reservation():
     assert _binding.fa_bwd_noalloc(0, *ptrs[1:], 1, 12, 128, 64, 1, 0.125, None) == fa.FA_ERR_INVALID_ARG
 
 
+# Head dim 128 takes 64-query tiles and a transposed dQ accumulator layout in the same
+# reservation; B1 H4 T777 (ragged last tile) exercises that layout.
+_WIDE_RAGGED = inputs.Workload("wide_ragged_t777", 1, 4, 777, 128, True, 11)
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("name,causal", [("tiny_causal", True), ("ragged_t1000", True),
-                                         ("ragged_t1000", False)])
+                                         ("ragged_t1000", False), ("wide_ragged_t777", True),
+                                         ("wide_ragged_t777", False)])
 def test_noalloc_matches_fa_bwd_twice_in_a_row(name, causal):
     import torch
-    w = inputs.WORKLOADS[name]
+    w = _WIDE_RAGGED if name == _WIDE_RAGGED.name else inputs.WORKLOADS[name]
     q, k, v = (t.cuda() for t in inputs.workload_qkv(w))
     do = inputs.workload_do(w).cuda()
     o, lse = fa.fwd(q, k, v, causal=causal)
