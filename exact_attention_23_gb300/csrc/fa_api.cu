@@ -162,6 +162,13 @@ int dense_forward(const void* q, const void* k, const void* v, void* o, float* l
   EncodeTiledFn enc = encode_fn();
   if (!enc) return FA_ERR_LAUNCH;
 
+  // Two 128-row Q tiles per CTA let the softmax of one overlap the MMAs of the other. When
+  // pairs would leave SMs idle (short sequences), one tile per CTA runs instead; in bf16 that
+  // is the kernel with double-buffered S and P (fa_fwd1_kernel.cuh), whose K steps overlap
+  // within the tile (B4 H12 T512: 7.7 against 9.4 us, inputs in L2).
+  const bool short_grid = n_pairs * BH < sms;
+  const bool one = short_grid && !qk8;
+
   fa::FwdLaunch a;
   a.p = fa::FwdParams{};  // the general-form fields stay zero on this path
   const bool maps_ok =
@@ -177,12 +184,6 @@ int dense_forward(const void* q, const void* k, const void* v, void* o, float* l
   a.p.status = status;
   a.p.T = T;
   a.p.BH = static_cast<int>(BH);
-  // Two 128-row Q tiles per CTA let the softmax of one overlap the MMAs of the other. When
-  // pairs would leave SMs idle (short sequences), one tile per CTA runs instead; in bf16 that
-  // is the kernel with double-buffered S and P (fa_fwd1_kernel.cuh), whose K steps overlap
-  // within the tile (B4 H12 T512: 7.7 against 9.4 us, inputs in L2).
-  const bool short_grid = n_pairs * BH < sms;
-  const bool one = short_grid && !qk8;
   const int tiles = (one || n_pairs * BH * 2 < sms) ? 1 : 2;
   const long long n_units = (tiles == 2) ? n_pairs : n_qt;
   a.p.n_units = static_cast<int>(n_units);

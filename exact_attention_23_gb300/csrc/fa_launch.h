@@ -8,6 +8,7 @@
 #include "fa_bwd_kernel.cuh"
 #include "fa_decode_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
+#include "fa_fwd1_kernel.cuh"
 
 namespace fa {
 
