@@ -140,6 +140,8 @@ KERNEL_SOURCES = {
     "decode": ("sm103.cuh", "fa_decode_kernel.cuh", "fa_decode.cu", "fa_fwd_ext_api.cu"),
     "block_sparse": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd_gen_d64.cu", "fa_fwd_ext_api.cu"),
     "fp8": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd_fp8.cu", "fa_api.cu"),
+    "fwd_t512": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd1_kernel.cuh", "fa_fwd1.cu", "fa_api.cu"),
+    "fwd_t1024": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd_d64.cu", "fa_api.cu"),
     "fwd_d128_causal": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd_d128.cu", "fa_api.cu"),
     "fwd_d128_full": ("sm103.cuh", "fa_fwd_kernel.cuh", "fa_fwd_d128.cu", "fa_api.cu"),
 }
@@ -150,6 +152,8 @@ TRAFFIC_RECORDS = {
     "decode": "dram_traffic_fa_decode_d64_b4h12_tk16384.json",
     "block_sparse": "dram_traffic_fa_fwd_block_sparse_d64_t8192.json",
     "fp8": "dram_traffic_fa_fwd_fp8_d128_causal_t16384.json",
+    "fwd_t512": "dram_traffic_fa_fwd1_d64_causal_b4h12_t512.json",
+    "fwd_t1024": "dram_traffic_fa_fwd_d64_causal_b4h12_t1024.json",
     "fwd_d128_causal": "dram_traffic_fa_fwd_d128_causal_b2h16_t16384.json",
     "fwd_d128_full": "dram_traffic_fa_fwd_d128_noncausal_b2h16_t16384.json",
 }
@@ -689,10 +693,12 @@ def run_gpu(args):
         ms = dom_ms if j == jdom else others[j]
         fl = fa.flops(B, H, T, D, True)
         by = fa.hbm_bytes(B, H, T, D)
+        rec = {512: "fwd_t512", 1024: "fwd_t1024", 16384: "fwd"}.get(T)
         per_T.append({"T": T, "ms": ms, "tflops": fl / ms / 1e9,
                       "frac_of_burst": fl / ms / 1e9 / bf16_peak,
                       "gbs": by / ms / 1e6, "frac_hbm": by / ms / 1e6 / hbm_peak,
-                      "input_sets": 1 if j == jdom else n_sets[j]})
+                      "input_sets": 1 if j == jdom else n_sets[j],
+                      "traffic": _measured_traffic(rec) if rec else None})
     dom = max(per_T, key=lambda r: fa.flops(B, H, r["T"], D, True))
 
     # ---- backward: the same sweep, K steps, dO drawn per T, workspace allocated up front
