@@ -20,7 +20,9 @@ so every launch reads inputs last touched a full step earlier.
 
 The same line carries `decode` (one query per head against a 16k-token KV cache, GB/s),
 `block_sparse` (T = 8192 with half the 128×128 blocks kept, TFLOP/s on kept blocks),
-`fp8_qk` (e4m3 queries and keys, bf16 values, B2 H16 T16384 d128, causal), `fwd_d128`
+`fp8_qk` (e4m3 queries and keys, bf16 values, B2 H16 T16384 d128, causal), `fwd_cta_pair`
+(the T = 16384 launch on CTA pairs that share each tensor-core product, beside the default
+kernel), `fwd_d128`
 (the wide-head workload B2 H16 T16384 d128, causal and non-causal), `context` (the figures
 the reference pages publish, with their hardware: context, not targets) and a
 `backward` object: the gradient pass (dQ, dK, dV through fa_bwd)
@@ -491,6 +493,30 @@ def _fwd_d128(args, fa, inputs, torch, dev, stream, bf16_peak, ws):
     return out
 
 
+def _fwd_cta_pair(args, fa, inputs, torch, dev, stream, bf16_peak, ws):
+    """The headline length (B4 H12 T16384 d64 causal, the sweep's seeded inputs) on CTA pairs
+    (fa_fwd_ex with FA_FLAG_CTA_PAIR: two CTAs of a cluster share every tensor-core product),
+    beside the default single-CTA kernel it is measured against; K calls each (<= 20)."""
+    T = SWEEP[-1]
+    q, k, v = (t.to(dev) for t in inputs.make_qkv(B, H, T, D, seed=3 + len(SWEEP) - 1))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+    steps = max(1, min(args.steps, 20))
+    out = {"workload": f"causal attention forward, bf16, B{B} H{H} T{T} d{D} on CTA pairs"}
+    for flags, key in ((fa.FA_FLAG_CTA_PAIR, "cta_pair"), (0, "single_cta")):
+        def call():
+            rc = fa.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              B, H, T, D, 1, D ** -0.5, None, 0, flags, stream.cuda_stream)
+            if rc != fa.FA_OK:
+                raise fa.FAError(rc, "fa_fwd_ex")
+        ms = _time_calls(call, steps, args.warmup, stream, torch, ws)
+        tf = ws * fa.flops(B, H, T, D, True) / ms / 1e9
+        out[key] = {"value": tf, "unit": "TFLOP/s", "ms_per_call": ms, "steps": steps,
+                    "frac_of_burst": tf / ws / bf16_peak}
+    out["gpu_launches"] = 2 * steps
+    return out
+
+
 def _general_forms(args, fa, inputs, torch, dev, stream, bf16_peak, hbm_peak, ws):
     """Decode (one new query per head against a 16k-token KV cache, B4 H12 d64, key range
     split over CTAs) and block-sparse self-attention (T = 8192, half of the 128×128 blocks
@@ -769,6 +795,8 @@ def run_gpu(args):
     extra["fp8_qk"] = _fwd_fp8(args, fa, inputs, torch, dev, stream, bf16_peak, ws)
     # ---- the wide-head workload's forward, causal and non-causal
     extra["fwd_d128"] = _fwd_d128(args, fa, inputs, torch, dev, stream, bf16_peak, ws)
+    # ---- the same headline launch on CTA pairs (an alternative kernel, not the default)
+    extra["fwd_cta_pair"] = _fwd_cta_pair(args, fa, inputs, torch, dev, stream, bf16_peak, ws)
 
     # ---- end to end: the C-ABI call on host buffers (fa_fwd_host: page-locked q, k, v in,
     # o, lse out; chunks of heads copied in, attended and copied back on overlapping

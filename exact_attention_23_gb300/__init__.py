@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     FA_ERR_UNSUPPORTED_DEVICE,
     FA_FLAG_TEST_STARVE_Q,
     FA_FLAG_TEST_STARVE_LATER_Q,
+    FA_FLAG_CTA_PAIR,
     FA_OK,
     FAError,
     fa_bwd,
@@ -63,7 +64,9 @@ def fwd(q, k, v, causal: bool = True, scale: float | None = None, out=None, lse=
     optional int32 CUDA tensor of one element, receives FA_ERR_TIMEOUT if an internal
     wait of the kernel ever gives up; ``timeout_ns`` bounds those waits (0: 2 s).
     ``flags`` is 0 except in tests of that path: FA_FLAG_TEST_STARVE_Q withholds every
-    query-tile load, FA_FLAG_TEST_STARVE_LATER_Q those after each CTA's first unit.
+    query-tile load, FA_FLAG_TEST_STARVE_LATER_Q those after each CTA's first unit; and
+    FA_FLAG_CTA_PAIR (d = 64) runs the forward on CTA pairs sharing each tensor-core product
+    (same results, slower on GB300 than the default).
     """
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):

@@ -22,6 +22,7 @@ FA_ERR_LAUNCH = 4
 FA_ERR_TIMEOUT = 5
 FA_FLAG_TEST_STARVE_Q = 1
 FA_FLAG_TEST_STARVE_LATER_Q = 2
+FA_FLAG_CTA_PAIR = 4
 FA_BWD_NOALLOC_SCRATCH_BYTES = 33554432
 
 # Every symbol include/fa.h declares.

@@ -127,6 +127,18 @@ bool encode_map_e4m3(EncodeTiledFn enc, CUtensorMap* map, const void* base, int 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over [B·H][T][64] bf16 values for the CTA-pair forward: boxes of 32 columns (64
+// bytes, the 64-byte swizzle span) × 128 rows × 1 head; each CTA of a pair loads one half.
+bool encode_map_v_half(EncodeTiledFn enc, CUtensorMap* map, const void* base, int T, int BH) {
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(T) * 128};
+  const cuuint32_t box[3] = {32, 128, 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Validation, tensor maps and launch of the dense forward; qk8: q and k are e4m3 codes.
 int dense_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                   int T, int d, int causal, float scale_log2, int* status,
@@ -136,7 +148,11 @@ int dense_forward(const void* q, const void* k, const void* v, void* o, float* l
   if (B <= 0 || H <= 0 || T <= 0) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale_log2)) return FA_ERR_INVALID_ARG;
-  if ((flags & ~static_cast<unsigned>(FA_FLAG_TEST_STARVE_Q | FA_FLAG_TEST_STARVE_LATER_Q)) != 0u)
+  if ((flags & ~static_cast<unsigned>(FA_FLAG_TEST_STARVE_Q | FA_FLAG_TEST_STARVE_LATER_Q |
+                                      FA_FLAG_CTA_PAIR)) != 0u)
+    return FA_ERR_INVALID_ARG;
+  const bool pair = (flags & FA_FLAG_CTA_PAIR) != 0u;
+  if (pair && (d != 64 || qk8 || (flags & (FA_FLAG_TEST_STARVE_Q | FA_FLAG_TEST_STARVE_LATER_Q))))
     return FA_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(B) * H;
   const long long n_qt = (static_cast<long long>(T) + 127) / 128;
@@ -167,7 +183,8 @@ int dense_forward(const void* q, const void* k, const void* v, void* o, float* l
   // is the kernel with double-buffered S and P (fa_fwd1_kernel.cuh), whose K steps overlap
   // within the tile (B4 H12 T512: 7.7 against 9.4 us, inputs in L2).
   const bool short_grid = n_pairs * BH < sms;
-  const bool one = short_grid && !qk8;
+  const bool one = short_grid && !qk8 && !pair;
+  const long long n_quads = (n_qt + 3) / 4;  // units of the CTA-pair kernel
 
   fa::FwdLaunch a;
   a.p = fa::FwdParams{};  // the general-form fields stay zero on this path
@@ -176,7 +193,10 @@ int dense_forward(const void* q, const void* k, const void* v, void* o, float* l
              encode_map_e4m3(enc, &a.tm_k, k, T, d, static_cast<int>(BH)))
           : (encode_map(enc, &a.tm_q, q, T, d, static_cast<int>(BH)) &&
              encode_map(enc, &a.tm_k, k, T, d, static_cast<int>(BH)));
-  if (!maps_ok || !encode_map(enc, &a.tm_v, v, T, d, static_cast<int>(BH)) ||
+  if (pair && !(encode_map(enc, &a.tm_k, k, T, d, static_cast<int>(BH), 64) &&
+                encode_map_v_half(enc, &a.tm_v, v, T, static_cast<int>(BH))))
+    return FA_ERR_INVALID_ARG;
+  if (!maps_ok || (!pair && !encode_map(enc, &a.tm_v, v, T, d, static_cast<int>(BH))) ||
       !encode_map(enc, &a.tm_o, o, T, d, static_cast<int>(BH), 32))
     return FA_ERR_INVALID_ARG;
   a.p.o = static_cast<__nv_bfloat16*>(o);
@@ -185,7 +205,7 @@ int dense_forward(const void* q, const void* k, const void* v, void* o, float* l
   a.p.T = T;
   a.p.BH = static_cast<int>(BH);
   const int tiles = (one || n_pairs * BH * 2 < sms) ? 1 : 2;
-  const long long n_units = (tiles == 2) ? n_pairs : n_qt;
+  const long long n_units = pair ? n_quads : (tiles == 2) ? n_pairs : n_qt;
   a.p.n_units = static_cast<int>(n_units);
   a.p.total_units = static_cast<int>(n_units * BH);
   // All heads interleaved in one cost-sorted list. (Limiting the interleave to the heads
@@ -200,11 +220,13 @@ int dense_forward(const void* q, const void* k, const void* v, void* o, float* l
   a.p.flags = flags;
   // Persistent: one CTA per SM (at most one per unit); each walks units blockIdx.x,
   // blockIdx.x + gridDim.x, ...
-  a.grid = static_cast<unsigned>(std::min<long long>(n_units * BH, sms));
+  a.grid = pair ? static_cast<unsigned>(2 * std::min<long long>(n_units * BH, sms / 2))
+              : static_cast<unsigned>(std::min<long long>(n_units * BH, sms));
   a.stream = static_cast<cudaStream_t>(stream);
 
   const cudaError_t e = qk8   ? fa::launch_fwd_fp8(a, d, causal != 0)
                         : one ? fa::launch_fwd1(a, d, causal != 0)
+                        : pair ? fa::launch_fwd_pair_d64(a, causal != 0)
                         : (d == 64) ? fa::launch_fwd_d64(a, causal != 0)
                                     : fa::launch_fwd_d128(a, causal != 0);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;

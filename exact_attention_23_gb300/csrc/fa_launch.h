@@ -9,6 +9,7 @@
 #include "fa_decode_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 #include "fa_fwd1_kernel.cuh"
+#include "fa_fwd_pair_kernel.cuh"
 
 namespace fa {
 
@@ -49,6 +50,10 @@ cudaError_t launch_fwd_fp8(const FwdLaunch& a, int d, bool causal);
 // One 128-row Q tile per CTA with double-buffered S and P (fa_fwd1_kernel.cuh); a.p holds one
 // tile per unit (tiles_per_cta = 1), d ∈ {64, 128}.
 cudaError_t launch_fwd1(const FwdLaunch& a, int d, bool causal);
+// Head dim 64 on CTA pairs (fa_fwd_pair_kernel.cuh): a.grid is even (clusters of two), a.p holds
+// groups of four Q tiles per unit, tm_k has 64-row boxes and tm_v 32-column × 128-row boxes
+// with the 64-byte swizzle.
+cudaError_t launch_fwd_pair_d64(const FwdLaunch& a, bool causal);
 
 // General form (Tq ≠ Tk, bottom-right causal, block masks, key ranges): the forward kernel
 // with GEN = true, then, when a.p.n_splits > 1, the merge of the partial results.

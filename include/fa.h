@@ -88,11 +88,18 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
  *                (FA_FLAG_TEST_STARVE_LATER_Q) omits them from each CTA's second work
  *                unit on, so that the waits run out after a first unit has finished.
  *                Both exist only to test the timeout path and produce NaN outputs.
+ *                Bit 2 (FA_FLAG_CTA_PAIR), d = 64 and bf16 only, runs the forward on CTA
+ *                pairs: two CTAs of a cluster share every tensor-core product (256 rows,
+ *                each CTA loading half of every K and V tile). Same results; on GB300 it
+ *                measures slower than the default single-CTA kernel (B4 H12 T16384
+ *                causal: 908 against 1017 TFLOP/s), so it is not the default. Not combined
+ *                with the test bits (FA_ERR_INVALID_ARG).
  *
  * Everything else as fa_fwd.
  */
 #define FA_FLAG_TEST_STARVE_Q 1u
 #define FA_FLAG_TEST_STARVE_LATER_Q 2u
+#define FA_FLAG_CTA_PAIR 4u
 int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
               int T, int d, int causal, float scale, int* status, unsigned long long timeout_ns,
               unsigned int flags, void* stream);

@@ -90,7 +90,10 @@ def _call(q=A, k=A + SZ, v=A + 2 * SZ, o=A + 3 * SZ, lse=A + 4 * SZ, B=1, H=1, T
     (dict(scale=0.0, q=A + 8), fa.FA_ERR_MISALIGNED),
     (dict(scale=-0.125, q=A + 8), fa.FA_ERR_MISALIGNED),
     (dict(scale=-1.0e30, q=A + 8), fa.FA_ERR_MISALIGNED),
-    (dict(flags=4), fa.FA_ERR_INVALID_ARG),
+    (dict(flags=8), fa.FA_ERR_INVALID_ARG),
+    (dict(flags=fa.FA_FLAG_CTA_PAIR, d=128), fa.FA_ERR_INVALID_ARG),   # pairs: head dim 64 only
+    (dict(flags=fa.FA_FLAG_CTA_PAIR | fa.FA_FLAG_TEST_STARVE_Q), fa.FA_ERR_INVALID_ARG),
+    (dict(flags=fa.FA_FLAG_CTA_PAIR, q=A + 8), fa.FA_ERR_MISALIGNED),  # accepted, then misaligned
     (dict(q=A + 8), fa.FA_ERR_MISALIGNED),
     (dict(o=A + 3 * SZ + 2), fa.FA_ERR_MISALIGNED),
     (dict(lse=A + 4 * SZ + 4), fa.FA_ERR_MISALIGNED),
