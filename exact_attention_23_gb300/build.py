@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfa.so")
 
-SOURCES = ["fa_api.cu", "fa_fwd1.cu", "fa_fwd_pair.cu", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_fwd_fp8.cu", "fa_fwd_gen_d64.cu",
+SOURCES = ["fa_api.cu", "fa_fwd1.cu", "fa_fwd1_gen.cu", "fa_fwd_pair.cu", "fa_fwd_d64.cu", "fa_fwd_d128.cu", "fa_fwd_fp8.cu", "fa_fwd_gen_d64.cu",
            "fa_fwd_gen_d128.cu", "fa_fwd_ext_api.cu", "fa_decode.cu", "fa_bwd_d64.cu", "fa_bwd_d128.cu",
            "fa_bwd_api.cu",
            "fa_noalloc.cu", "fa_hostio.cu"]

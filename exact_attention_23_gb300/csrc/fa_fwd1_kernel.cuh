@@ -19,7 +19,11 @@
 // free, and the tensor core always has the next product queued.
 //
 // Work unit = one (batch·head, 128-row Q tile), heaviest first, zig-zag over a persistent grid
-// (one CTA per SM). 224 threads, 7 warps:
+// (one CTA per SM). The general form (GEN: queries against a longer key sequence with
+// bottom-right causal visibility, a key range per unit, a block mask) walks, per unit, only
+// the K tiles of its range that its rows use, and writes the range's normalised fp32 row and
+// LSE when the key range is split (merged afterwards by fa_fwd_combine_kernel). 224 threads,
+// 7 warps:
 //   warps 0-3  softmax: thread t owns query row t = TMEM lane t (the whole row of S)
 //   warp  4    S issuer: S(j) = Q·K(j)ᵀ into S[j mod 2] (one elected thread); TMEM owner
 //   warp  5    TMA producer (Q per unit; K and V per step through a ring)
@@ -88,7 +92,7 @@ struct Bars1 {
 };
 static_assert(sizeof(Bars1) <= 256, "barrier block");
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool GEN = false>
 __global__ void __launch_bounds__(kThreads1, 1)
     fa_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
     for (int r = 0; ok && r * grid < p.total_units; ++r) {
       const int L = unit_index(r, cta, grid);
       if (L >= p.total_units) continue;
-      const Unit u = unit_of<CAUSAL, false>(p, L);
+      const Unit u = unit_of<CAUSAL, GEN>(p, L);
       const int qb = qn & 1;
       if (qn >= 2 && !mbar_wait_warp(&bars->q_empty[qb], ((qn >> 1) - 1) & 1, wc)) { ok = false; break; }
       const bool load = load_q && (later_q || qn == 0);
@@ -170,7 +174,9 @@ __global__ void __launch_bounds__(kThreads1, 1)
       }
       __syncwarp();
       ++qn;
+      int kt = u.kb - 1;
       for (int j = 0; j < u.n_steps; ++j, ++g) {
+        kt = next_kt<CAUSAL, GEN>(p, u, kt, 0);  // (dense: kt = j)
         const int st = g % C::kStages;
         const int use = g / C::kStages;
         if (use > 0 && !mbar_wait_warp(&bars->kv_empty[st], (use - 1) & 1, wc)) { ok = false; break; }
@@ -179,12 +185,12 @@ __global__ void __launch_bounds__(kThreads1, 1)
 #pragma unroll
           for (int s = 0; s < C::kSub; ++s)
             tma_load_3d_hint(smem + C::kKOff + st * C::kTileBytes + s * C::kSubBytes, &tm_k,
-                             &bars->k_full[st], s * 64, j * kBlockN, u.bh, keep);
+                             &bars->k_full[st], s * 64, kt * kBlockN, u.bh, keep);
           mbar_arrive_expect_tx(&bars->v_full[st], C::kTileBytes);
 #pragma unroll
           for (int s = 0; s < C::kSub; ++s)
             tma_load_3d_hint(smem + C::kVOff + st * C::kTileBytes + s * C::kSubBytes, &tm_v,
-                             &bars->v_full[st], s * 64, j * kBlockN, u.bh, keep);
+                             &bars->v_full[st], s * 64, kt * kBlockN, u.bh, keep);
         }
         __syncwarp();
       }
@@ -217,7 +223,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
       for (int r = 0; ok && r * grid < p.total_units; ++r) {
         const int L = unit_index(r, cta, grid);
         if (L >= p.total_units) continue;
-        const Unit u = unit_of<CAUSAL, false>(p, L);
+        const Unit u = unit_of<CAUSAL, GEN>(p, L);
         const int qb = qn & 1;
         if (!mbar_wait_warp(&bars->q_full[qb], (qn >> 1) & 1, wc)) { ok = false; break; }
         for (int j = 0; j < u.n_steps; ++j, ++g) {
@@ -258,7 +264,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
       for (int r = 0; ok && r * grid < p.total_units; ++r) {
         const int L = unit_index(r, cta, grid);
         if (L >= p.total_units) continue;
-        const Unit u = unit_of<CAUSAL, false>(p, L);
+        const Unit u = unit_of<CAUSAL, GEN>(p, L);
         for (int j = 0; j < u.n_steps; ++j, ++g) {
           const int st = g % C::kStages;
           const int b = g & 1;
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
           __syncwarp();
           FA1_TRACE(14, j);
         }
-        ++nunits;
+        if (u.n_steps > 0) ++nunits;  // (a general-form unit may use no K tile: no P·V)
       }
     }
     // Nothing may still be running on the tensor core when TMEM is released.
@@ -300,26 +306,54 @@ __global__ void __launch_bounds__(kThreads1, 1)
 
     int g = 0;  // K steps consumed so far over this CTA's units
     bool ok = true;
+    // Where a unit's rows go: the bf16 output (row_idx; r0 = the warp's first row, for the
+    // TMA store) and LSE, or (general form with several key ranges) the fp32 partial row
+    // and LSE of its range (part_idx).
     struct RowOut {
-      size_t row_idx;
+      size_t row_idx, part_idx;
       int r0, bh;
-      bool in_range;
+      bool in_range, partial;
+    };
+    auto row_out = [&](int bh, int split, int r0) {
+      const int q_row = r0 + lane;
+      return RowOut{static_cast<size_t>(bh) * static_cast<size_t>(p.T) + static_cast<size_t>(q_row),
+                    (static_cast<size_t>(split) * p.BH + bh) * static_cast<size_t>(p.T) +
+                        static_cast<size_t>(q_row),
+                    r0, bh, q_row < p.T, GEN && p.n_splits > 1};
+    };
+    auto write_lse = [&](const RowOut& w, float v) {
+      if (!w.in_range) return;
+      if (w.partial) p.lse_part[w.part_idx] = v;
+      else p.lse[w.row_idx] = v;
+    };
+    // A row that saw no key (general form: O = 0, LSE = −∞) or a failed unit (NaN).
+    auto write_const_row = [&](const RowOut& w, uint32_t bits) {
+      if (!w.in_range) return;
+      if (w.partial) {
+        float4* prow = reinterpret_cast<float4*>(p.o_part + w.part_idx * D);
+        const float f = u2f(bits);
+#pragma unroll
+        for (int t = 0; t < D / 4; ++t) prow[t] = make_float4(f, f, f, f);
+      } else {
+        uint4* orow = reinterpret_cast<uint4*>(p.o + w.row_idx * D);
+        const uint32_t b2 = pack_bf16x2(u2f(bits), u2f(bits));
+#pragma unroll
+        for (int t = 0; t < D / 8; ++t) orow[t] = make_uint4(b2, b2, b2, b2);
+      }
     };
     auto fail_rows = [&](const RowOut& w) {
-      if (!w.in_range) return;
-      uint4* orow = reinterpret_cast<uint4*>(p.o + w.row_idx * D);
-      const uint32_t nan2 = 0x7FC07FC0u;
-#pragma unroll
-      for (int t = 0; t < D / 8; ++t) orow[t] = make_uint4(nan2, nan2, nan2, nan2);
-      p.lse[w.row_idx] = __uint_as_float(0x7FC00000u);
+      write_const_row(w, 0x7FC00000u);
+      write_lse(w, __uint_as_float(0x7FC00000u));
     };
     // The finished unit's O (TMEM, after its last P·V) to the output: read 32 columns at a
     // time, scale by 1/l, stage in this warp's 4 KB slice in the O map's 128-byte-swizzled
     // layout (16-byte chunk c of row r at c ^ (r mod 8)), one TMA store per 64 columns; rows
     // past the sequence are not written. O is released to the next unit's first P·V as soon
     // as it has been read.
+    // (General form: a row that saw no key of the range has l = 0 and gets O = 0, LSE = −∞;
+    // partial rows go out as fp32, each thread writing its own row.)
     auto epilogue = [&](const RowOut& w, float l, float m) {
-      const float inv_l = 1.0f / l;
+      const float inv_l = (GEN && !(l > 0.0f)) ? 0.0f : 1.0f / l;
       uint8_t* slice = smem + C::kOOff + warp * 4096;
       const uint32_t ob = smem_u32(slice) + lane * 128;
 #pragma unroll 1
@@ -334,6 +368,16 @@ __global__ void __launch_bounds__(kThreads1, 1)
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->o_free);
+        }
+        if (GEN && w.partial) {
+          if (w.in_range) {
+            float4* prow = reinterpret_cast<float4*>(p.o_part + w.part_idx * D + hb * 64);
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+              prow[t] = make_float4(u2f(o[4 * t]) * inv_l, u2f(o[4 * t + 1]) * inv_l,
+                                    u2f(o[4 * t + 2]) * inv_l, u2f(o[4 * t + 3]) * inv_l);
+          }
+          continue;
         }
         if (lane == 0) bulk_wait_group_read0();  // the slice's previous store has read it
         __syncwarp();
@@ -351,20 +395,20 @@ __global__ void __launch_bounds__(kThreads1, 1)
           bulk_commit_group();
         }
       }
-      if (w.in_range) p.lse[w.row_idx] = (m + log2f(l)) * 0.69314718055994530942f;
+      write_lse(w, (GEN && !(l > 0.0f)) ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f);
     };
     // The pending (finished, not yet written) unit's l, m and output position wait in this
     // thread's 16-byte record in shared memory, not in registers the step loop needs.
     bool pend = false;
     float4* const prec = reinterpret_cast<float4*>(smem + C::kPendOff) + row;
+    // (.w = bh + BH·split)
     auto parked = [&](float& l, float& m) {
       const float4 v = *prec;
       l = v.x;
       m = v.y;
-      const int r0 = __float_as_int(v.z), bh = __float_as_int(v.w);
-      const int q_row = r0 + lane;
-      return RowOut{static_cast<size_t>(bh) * static_cast<size_t>(p.T) + static_cast<size_t>(q_row),
-                    r0, bh, q_row < p.T};
+      const int r0 = __float_as_int(v.z), hs = __float_as_int(v.w);
+      const int split = GEN ? hs / p.BH : 0;
+      return row_out(hs - split * p.BH, split, r0);
     };
     auto fail_pending = [&]() {
       float l, m;
@@ -388,28 +432,43 @@ __global__ void __launch_bounds__(kThreads1, 1)
     for (int r = 0; r * grid < p.total_units; ++r) {
       const int L = unit_index(r, cta, grid);
       if (L >= p.total_units) continue;
-      const Unit u = unit_of<CAUSAL, false>(p, L);
+      const Unit u = unit_of<CAUSAL, GEN>(p, L);
       const int n = u.nkv[0];
       const int qt = u.qt0;
       const int q_row = qt * kBlockM + row;
-      const RowOut cur{static_cast<size_t>(u.bh) * static_cast<size_t>(p.T) + static_cast<size_t>(q_row),
-                       qt * kBlockM + warp * 32, u.bh, q_row < p.T};
+      const RowOut cur = row_out(u.bh, u.split, qt * kBlockM + warp * 32);
       if (!ok) {
         if (pend) fail_pending();
         fail_rows(cur);
         continue;
       }
+      if (GEN && n == 0) {  // the unit uses no K tile of its range
+        if (pend) flush_pending();
+        write_const_row(cur, 0u);
+        write_lse(cur, -INFINITY);
+        continue;
+      }
       float m_ref = -INFINITY;  // reference max (base-2 scaled units) shared by O and l
       float l = 0.0f;
+      int kt = u.kb - 1;
       for (int j = 0; j < n; ++j, ++g) {
+        kt = next_kt<CAUSAL, GEN>(p, u, kt, 0);  // (dense: kt = j)
         const int b = g & 1;
         if (!mbar_wait_warp(&bars->s_full[b], (g >> 1) & 1, wc)) { ok = false; break; }
         FA1_TRACE(30, j);
         tc_fence_after_sync();
-        const int k0 = j * kBlockN;
-        // Keys past the end of the sequence, and (causal) keys after this query.
-        const int lim = (CAUSAL ? min(q_row + 1, p.T) : p.T) - k0;
-        const bool masked = (CAUSAL && j == qt) || (k0 + kBlockN > p.T);
+        const int k0 = kt * kBlockN;
+        // Keys past the end of the sequence, and (causal) keys after this query (general
+        // form: after query + Tk − Tq).
+        int lim;
+        bool masked;
+        if constexpr (GEN) {
+          lim = (CAUSAL ? min(q_row + 1 + p.kv_off, p.Tk) : p.Tk) - k0;
+          masked = lim < kBlockN;
+        } else {
+          lim = (CAUSAL ? min(q_row + 1, p.T) : p.T) - k0;
+          masked = (CAUSAL && kt == qt) || (k0 + kBlockN > p.T);
+        }
         uint32_t s[kBlockN];
         const uint32_t t_s = tmem + lane_off + C::col_s(b);
         tmem_ld32(t_s + 0, s);
@@ -454,9 +513,11 @@ __global__ void __launch_bounds__(kThreads1, 1)
         const bool any_rescale = __any_sync(0xffffffffu, rescale);
         FA1_TRACE(40, j);
 
-        // p = 2^(s·c − m_ref) on fp32 pairs; row sum in fp32; P kept as bf16 pairs.
+        // p = 2^(s·c − m_ref) on fp32 pairs; row sum in fp32; P kept as bf16 pairs. (General
+        // form: a row that has seen no key yet has m_ref = −∞ and all its p are 0.)
         const uint64_t c2 = f2_pack(c, c);
-        const uint64_t nm2 = f2_pack(-m_ref, -m_ref);
+        const float m_use = (GEN && m_ref == -INFINITY) ? 0.0f : m_ref;
+        const uint64_t nm2 = f2_pack(-m_use, -m_use);
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
         uint32_t pk[kBlockN / 2];
 #pragma unroll
@@ -529,7 +590,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
         fail_rows(cur);
         continue;
       }
-      *prec = make_float4(l, m_ref, __int_as_float(cur.r0), __int_as_float(cur.bh));
+      *prec = make_float4(l, m_ref, __int_as_float(cur.r0), __int_as_float(cur.bh + p.BH * u.split));
       pend = true;
     }
     if (pend) flush_pending();  // the last unit's epilogue (its last step is g − 1)

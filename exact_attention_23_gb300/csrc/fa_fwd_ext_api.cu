@@ -19,14 +19,24 @@ namespace {
 
 size_t round_up256(size_t x) { return (x + 255u) / 256u * 256u; }
 
-// Key ranges per query unit when the caller asks for automatic choice: enough CTAs to
-// cover every SM twice, at least two K tiles per range, at most 64 ranges.
+// Key ranges per query tile when the caller asks for automatic choice. The units (query
+// tile, range) run one per SM at a time, so a choice of s ranges costs about ⌈units·s / SMs⌉
+// rounds of (K tiles per range + about one tile's worth of set-up and output). More ranges
+// must be at least 5 % cheaper than fewer (partial rows and their merge cost memory
+// traffic); at most 64.
 int auto_splits(long long BH, long long n_qt, long long n_kt, int sms) {
   const long long units = BH * n_qt;
-  if (units >= sms) return 1;
-  long long s = (2LL * sms + units - 1) / units;
-  s = std::min<long long>(s, std::max<long long>(1, n_kt / 2));
-  return static_cast<int>(std::max<long long>(1, std::min<long long>(s, 64)));
+  long long best = 1, best_cost = -1;
+  for (long long s = 1; s <= std::min<long long>(64, n_kt); ++s) {
+    const long long per = (n_kt + s - 1) / s;
+    const long long used = (n_kt + per - 1) / per;  // no empty range
+    const long long cost = (units * used + sms - 1) / sms * (per + 1);
+    if (best_cost < 0 || cost * 20 < best_cost * 19) {
+      best_cost = cost;
+      best = used;
+    }
+  }
+  return static_cast<int>(best);
 }
 
 // Decode (one query row per head): as many key ranges as fit one wave of resident CTAs
@@ -37,12 +47,21 @@ int decode_splits(long long BH, long long Tk, int sms) {
   return static_cast<int>(std::max<long long>(1, std::min<long long>(s, 1024)));
 }
 
+// Two query rows (multi-query decode): two warps per row, two rows per CTA; key ranges so
+// that B·H × ranges CTAs fill one wave (two per SM), each range at least 256 keys.
+int multi_splits(long long BH, long long Tk, int sms) {
+  long long s = static_cast<long long>(sms) * fa::kDecMultiCtasPerSm / BH;
+  s = std::min<long long>(s, std::max<long long>(1, Tk / 256));
+  return static_cast<int>(std::max<long long>(1, std::min<long long>(s, 1024)));
+}
+
 // Key ranges actually used for these sizes (requested > 0, or the automatic choice), with
 // no empty range.
 int effective_splits(long long BH, long long Tq, long long Tk, int requested, int sms) {
   const long long n_qt = (Tq + 127) / 128, n_kt = (Tk + 127) / 128;
-  if (Tq == 1) {
-    long long s = requested ? requested : decode_splits(BH, Tk, sms);
+  if (Tq <= fa::kDecMultiMaxRows) {
+    long long s = requested ? requested
+                            : (Tq == 1 ? decode_splits(BH, Tk, sms) : multi_splits(BH, Tk, sms));
     s = std::min<long long>(s, Tk);
     const long long per = (Tk + s - 1) / s;
     return static_cast<int>((Tk + per - 1) / per);
@@ -129,8 +148,11 @@ int launch_general(const GenArgs& g, int sms) {
   a.grid = static_cast<unsigned>(std::min<long long>(a.p.total_units, sms));
   a.stream = static_cast<cudaStream_t>(g.stream);
   const unsigned combine_grid = static_cast<unsigned>(sms) * 8u;
-  const cudaError_t e = (g.d == 64) ? fa::launch_fwd_gen_d64(a, g.causal != 0, combine_grid)
-                                    : fa::launch_fwd_gen_d128(a, g.causal != 0, combine_grid);
+  // One Q tile per unit: the one-tile kernel, whose S and P are double-buffered, overlaps
+  // consecutive K steps of its single tile.
+  const cudaError_t e = (tiles == 1) ? fa::launch_fwd1_gen(a, g.d, g.causal != 0, combine_grid)
+                        : (g.d == 64) ? fa::launch_fwd_gen_d64(a, g.causal != 0, combine_grid)
+                                      : fa::launch_fwd_gen_d128(a, g.causal != 0, combine_grid);
   return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -224,6 +246,34 @@ int fa_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, 
     if (BH * splits > INT32_MAX) return FA_ERR_INVALID_ARG;
     const cudaError_t e = fa::launch_decode(dp, d, static_cast<unsigned>(sms) * 8u,
                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  }
+  if (Tq <= fa::kDecMultiMaxRows) {
+    // Two query rows per head: two CUDA-core warps per row, the four warps sharing every
+    // K/V chunk (a 128-row tensor tile would be nearly all padding).
+    fa::DecodeParams dp{};
+    dp.q = static_cast<const __nv_bfloat16*>(q);
+    dp.k = static_cast<const __nv_bfloat16*>(k);
+    dp.v = static_cast<const __nv_bfloat16*>(v);
+    dp.o = static_cast<__nv_bfloat16*>(o);
+    dp.lse = lse;
+    dp.BH = static_cast<int>(BH);
+    dp.Tk = Tk;
+    dp.Tq = Tq;
+    dp.causal = causal ? 1 : 0;
+    dp.n_splits = splits;
+    dp.keys_per_split = static_cast<int>((static_cast<long long>(Tk) + splits - 1) / splits);
+    dp.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+    if (splits > 1) {
+      uint8_t* ws = static_cast<uint8_t*>(workspace);
+      dp.o_part = reinterpret_cast<float*>(ws);
+      dp.lse_part = reinterpret_cast<float*>(
+          ws + round_up256(static_cast<size_t>(splits) * BH * Tq * d * 4));
+    }
+    if (BH * splits > INT32_MAX) return FA_ERR_INVALID_ARG;
+    const cudaError_t e = fa::launch_decode_multi(dp, d,
+                                                  static_cast<unsigned>(sms) * 8u,
+                                                  static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
   }
   GenArgs g{q, k, v, o, lse, nullptr, 1, B, H, Tq, Tk, d, causal, scale, splits, workspace,

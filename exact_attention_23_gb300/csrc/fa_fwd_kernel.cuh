@@ -206,12 +206,13 @@ template <bool CAUSAL, bool GEN>
 __device__ __forceinline__ Unit unit_of(const FwdParams& p, int L) {
   Unit u;
   if constexpr (GEN) {
-    // bh fastest, then key range, then query unit (no cost order: ranges are balanced)
+    // bh fastest, then key range, then query unit, the last query unit first (under the
+    // causal mask later query tiles see more keys: the heaviest units go out first)
     const int rest = static_cast<int>(p.div_bh.div(static_cast<uint32_t>(L)));
     u.bh = L - rest * p.BH;
     const int qu = static_cast<int>(p.div_splits.div(static_cast<uint32_t>(rest)));
     u.split = rest - qu * p.n_splits;
-    u.qt0 = qu * p.tiles_per_cta;
+    u.qt0 = (p.n_units - 1 - qu) * p.tiles_per_cta;
     u.kb = u.split * p.kt_per_split;
     u.ke = min(p.n_kv, u.kb + p.kt_per_split);
     u.mh = (p.bmask_heads == 1) ? 0 : u.bh;

@@ -50,6 +50,9 @@ cudaError_t launch_fwd_fp8(const FwdLaunch& a, int d, bool causal);
 // One 128-row Q tile per CTA with double-buffered S and P (fa_fwd1_kernel.cuh); a.p holds one
 // tile per unit (tiles_per_cta = 1), d ∈ {64, 128}.
 cudaError_t launch_fwd1(const FwdLaunch& a, int d, bool causal);
+// The general form (queries against a longer key sequence, key ranges, block mask) on the
+// one-tile kernel (tiles_per_cta = 1), then the merge when the key range is split.
+cudaError_t launch_fwd1_gen(const FwdLaunch& a, int d, bool causal, unsigned combine_grid);
 // Head dim 64 on CTA pairs (fa_fwd_pair_kernel.cuh): a.grid is even (clusters of two), a.p holds
 // groups of four Q tiles per unit, tm_k has 64-row boxes and tm_v 32-column × 128-row boxes
 // with the 64-byte swizzle.
@@ -63,6 +66,12 @@ cudaError_t launch_fwd_gen_d128(const FwdLaunch& a, bool causal, unsigned combin
 // Decode (Tq = 1) on the CUDA cores: grid B·H × n_splits, then the merge when split.
 cudaError_t launch_decode(const DecodeParams& p, int d, unsigned combine_grid,
                           cudaStream_t stream);
+// Two query rows per head (Tq = kDecMultiMaxRows) on the CUDA cores, two warps per row: grid
+// B·H × n_splits, then the merge when split. (From three rows on, the one-tile tensor-core
+// kernel is faster.)
+constexpr int kDecMultiMaxRows = 2;
+cudaError_t launch_decode_multi(const DecodeParams& p, int d, unsigned combine_grid,
+                                cudaStream_t stream);
 
 struct BwdLaunch {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;

@@ -123,13 +123,15 @@ int fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, 
 /*
  * fa_fwd_kv — Tq queries against Tk keys, e.g. new tokens (or one decoded token,
  * Tq = 1) against the K/V of every earlier token, which generation keeps ("手写
- * FlashAttention" step ①). causal requires Tq ≤ Tk. When B·H·ceil(Tq/128) query tiles
- * leave SMs idle, the key range is split into n_splits ranges processed by different
- * CTAs; each writes a partial result (normalised O, LSE) to the workspace and a second
+ * FlashAttention" step ①). causal requires Tq ≤ Tk. One or two query rows run on the CUDA
+ * cores (a dot product and a scaled add per cached row, which a 128-row tensor tile would
+ * mostly pad); more run on the tensor cores. When the CTAs of either leave SMs idle, the
+ * key range is split into n_splits ranges processed by different CTAs; each writes a partial result (normalised O, LSE) to the workspace and a second
  * kernel merges them with weights exp(LSE_s − max LSE) — the merge over K/V blocks that
  * step ③ of the same page attributes to the first FlashAttention's outer loop.
  *
  *   n_splits  : key ranges; 0 picks a number from the SM count of the current device
+ *               (ranges count keys for Tq ≤ 2 and 128-key tiles above)
  *   workspace : device memory, 256-byte aligned, at least fa_fwd_kv_workspace_size(...)
  *               bytes, owned by the caller; unused (may be NULL) when one range is used.
  *               Must not overlap any argument or be used by a concurrent call.

@@ -1,6 +1,6 @@
 """GPU parity of the general forward forms against the fp64 oracle's general form:
 fa_fwd_kv (Tq queries over Tk keys, bottom-right causal, key range split over CTAs with
-the partial results merged; Tq = 1 runs the CUDA-core decode kernel) and
+the partial results merged; Tq ≤ 2 runs the CUDA-core decode kernels) and
 fa_fwd_block_sparse (128×128 blocks switched off).
 
 Tolerances as for the forward: O max-abs ≤ 2e-2, mean-abs ≤ 1e-3 (+ 2⁻⁹·mean|O_ref| for
@@ -49,6 +49,18 @@ def _qkv_kv(B, H, Tq, Tk, d, seed):
     (1, 4, 1, 777, 64, True, 0),       # ragged cache length
     (1, 8, 1, 1000, 128, False, 0),
     (2, 4, 7, 2000, 64, True, 3),
+    # two query rows (the CUDA-core multi-query decode): single and split key ranges, a tiny
+    # cache; then the first tensor-core sizes
+    (2, 12, 2, 4096, 64, True, 0),
+    (1, 4, 2, 3000, 128, False, 5),
+    (1, 4, 2, 5, 64, True, 0),         # fewer cached keys than a chunk
+    (1, 4, 3, 5, 64, True, 0),         # fewer cached keys than a chunk
+    (2, 6, 4, 3000, 128, True, 1),
+    (1, 3, 4, 4, 64, True, 3),         # Tq = Tk = 4: plain causal attention, more ranges than keys allow
+    (1, 4, 5, 777, 64, False, 0),
+    (2, 3, 8, 8192, 64, True, 0),
+    (1, 3, 9, 9, 128, True, 0),
+    (2, 4, 16, 2500, 64, True, 7),
     (1, 4, 128, 1024, 64, True, 0),
     (1, 4, 200, 1500, 128, True, 0),   # two query tiles, ragged
     (1, 2, 300, 300, 64, True, 0),     # Tq = Tk: plain causal attention

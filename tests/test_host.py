@@ -236,7 +236,10 @@ def test_fwd_kv_workspace_size(lib):
     assert fa.fa_fwd_kv_workspace_size(2, 12, 1, 4096, 64, 4) == (
         -(-4 * 24 * 64 * 4 // 256) * 256 + -(-4 * 24 * 4 // 256) * 256)
     assert fa.fa_fwd_kv_workspace_size(2, 12, 1, 4096, 64, 1) == 1   # no workspace needed
-    assert fa.fa_fwd_kv_workspace_size(1, 1, 2, 100, 64, 8) == 1     # one K tile: one range
+    assert fa.fa_fwd_kv_workspace_size(1, 1, 3, 100, 64, 8) == 1     # one K tile: one range
+    # two query rows run on the CUDA cores, whose key ranges count keys, not K tiles:
+    # 8 ranges of 13 keys, S·B·H·Tq·d·4 + S·B·H·Tq·4 bytes, 256-aligned
+    assert fa.fa_fwd_kv_workspace_size(1, 1, 2, 100, 64, 8) == 8 * 2 * 64 * 4 + 256
     # one query row (decode): ranges are counted in keys; 100 keys in 8 ranges of 13
     assert fa.fa_fwd_kv_workspace_size(1, 1, 1, 100, 64, 8) == 8 * 64 * 4 // 256 * 256 + 256
     assert fa.fa_fwd_kv_workspace_size(1, 1, 1, 3, 64, 8) == 3 * 64 * 4 + 256  # at most Tk ranges
