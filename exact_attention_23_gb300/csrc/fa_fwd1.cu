@@ -20,7 +20,7 @@ static cudaError_t launch1(const FwdLaunch& a) {
     if (e != cudaSuccess) return e;
     done[dev / 64].fetch_or(bit, std::memory_order_acq_rel);
   }
-  return launch_pdl(fn, a.grid, kThreads1, smem, a.stream, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
+  return launch_pdl(fn, a.grid, Cfg1<D>::kThreads, smem, a.stream, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
 }
 
 cudaError_t launch_fwd1(const FwdLaunch& a, int d, bool causal) {

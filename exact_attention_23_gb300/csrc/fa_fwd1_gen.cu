@@ -21,7 +21,7 @@ static cudaError_t launch1g(const FwdLaunch& a, unsigned combine_grid) {
     if (e != cudaSuccess) return e;
     done[dev / 64].fetch_or(bit, std::memory_order_acq_rel);
   }
-  cudaError_t e = launch_pdl(fn, a.grid, kThreads1, smem, a.stream, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
+  cudaError_t e = launch_pdl(fn, a.grid, Cfg1<D>::kThreads, smem, a.stream, a.tm_q, a.tm_k, a.tm_v, a.tm_o, a.p);
   if (e != cudaSuccess || a.p.n_splits <= 1) return e;
   const float* op = a.p.o_part;
   const float* lp = a.p.lse_part;

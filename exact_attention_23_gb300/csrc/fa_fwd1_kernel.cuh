@@ -22,17 +22,27 @@
 // (one CTA per SM). The general form (GEN: queries against a longer key sequence with
 // bottom-right causal visibility, a key range per unit, a block mask) walks, per unit, only
 // the K tiles of its range that its rows use, and writes the range's normalised fp32 row and
-// LSE when the key range is split (merged afterwards by fa_fwd_combine_kernel). 224 threads,
-// 7 warps:
-//   warps 0-3  softmax: thread t owns query row t = TMEM lane t (the whole row of S)
-//   warp  4    S issuer: S(j) = Q·K(j)ᵀ into S[j mod 2] (one elected thread); TMEM owner
-//   warp  5    TMA producer (Q per unit; K and V per step through a ring)
-//   warp  6    P·V issuer: O += P(j)·V(j) from P[j mod 2]
-// With 224 threads every thread may hold 255 registers: the softmax keeps the whole S row,
-// its P and its state in registers without spilling.
+// LSE when the key range is split (merged afterwards by fa_fwd_combine_kernel).
+//
+// Softmax halves (H = 2 at D = 64, H = 1 at D = 128). At D = 64 each query row's 128 keys of
+// a step are split over two warps that own the same TMEM lanes: warp q (q = 0…3) takes keys
+// 0–63 and warp q + 4 keys 64–127 of every K tile, and each half keeps its own running max,
+// sum and O accumulator over its keys — the tiled scan of step ③ of the same page applied to
+// two interleaved key subsets — so the two warps never meet inside the step loop. They merge
+// once per unit (O = (2^(m₀−m)·O₀ + 2^(m₁−m)·O₁) / (2^(m₀−m)·l₀ + 2^(m₁−m)·l₁), m = max(m₀, m₁)),
+// exchanging m and l through shared memory. Two softmax warps per SM sub-partition hide each
+// other's latency, where one warp with a whole 128-key row sat in its own dependency chains.
+// Warps (32·(4H + 3) threads):
+//   warps 0 … 4H−1  softmax: warp w owns query rows 32(w mod 4) … +31 (TMEM lanes) and the
+//                   keys 64·(w div 4) … of each step when H = 2
+//   warp  4H        S issuer: S(j) = Q·K(j)ᵀ into S[j mod 2] (one elected thread); TMEM owner
+//   warp  4H + 1    TMA producer (Q per unit; K and V per step through a ring)
+//   warp  4H + 2    P·V issuer: O_h += P_h(j)·V_h(j) from P[j mod 2]
+// With 224 threads (H = 1) every thread may hold 255 registers, with 352 (H = 2) 184: either
+// way the softmax keeps its part of the S row, its P and its state in registers.
 // Tensor memory (512 columns × 128 lanes × 32 bit):
-//   [0,128) S[0]   [128,256) S[1]   [256,256+D) O (fp32)   then P[0], P[1] (64 columns each:
-//   128 keys as bf16 pairs) — 448 columns at D = 64, 512 at D = 128.
+//   [0,128) S[0]   [128,256) S[1]   [256,256+H·D) O_0 … O_{H−1} (fp32)   then P[0], P[1] (64
+//   columns each: 128 keys as bf16 pairs, half h in columns 32h … of each) — 512 columns.
 // Every barrier phase is counted over the CTA's whole list of units, so units follow one
 // another with no re-initialisation; a unit's epilogue (O / l to bf16 through shared memory
 // and a TMA store, and the LSE) is deferred into the first step of the next unit.
@@ -47,11 +57,17 @@
 
 namespace fa {
 
-constexpr int kThreads1 = 224;
-
 template <int D>
 struct Cfg1 {
   static_assert(D == 64 || D == 128, "head dim");
+  // Softmax halves: two O accumulators fit tensor memory at D = 64 only.
+  static constexpr int kHalves = (D == 64) ? 2 : 1;
+  static constexpr int kCols = kBlockN / kHalves;        // keys per softmax warp and step
+  static constexpr int kSoftWarps = 4 * kHalves;
+  static constexpr int kWarpS = kSoftWarps;              // S issuer, TMEM owner
+  static constexpr int kWarpLoad = kSoftWarps + 1;       // TMA producer
+  static constexpr int kWarpPV = kSoftWarps + 2;         // P·V issuer
+  static constexpr int kThreads = (kSoftWarps + 3) * 32;
   // K/V ring depth: four stages at D = 64; D = 128 tiles are twice the size, two fit.
   static constexpr int kStages = (D == 64) ? 4 : 2;
   static_assert(kStages >= 2 && kStages <= 4, "K/V ring depth (barrier arrays hold 4)");
@@ -68,11 +84,16 @@ struct Cfg1 {
   static constexpr int kOBytes = 4 * 4096;
   // Each softmax thread's deferred epilogue record (l, m, first row of its warp, head).
   static constexpr int kPendOff = kOOff + kOBytes;
-  static constexpr int kBarOff = kPendOff + kBlockM * 16;
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // barriers + 1 KB alignment slack
+  // The halves' (m, l) exchange at the end of a unit, double-buffered by unit parity.
+  static constexpr int kXchOff = kPendOff + kHalves * kBlockM * 16;
+  static constexpr int kBarOff = kXchOff + 2 * kHalves * kBlockM * 8;
+  static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // barriers + 1 KB alignment slack
   static __host__ __device__ constexpr uint32_t col_s(int b) { return b ? 128u : 0u; }
-  static constexpr uint32_t kColO = 256u;
-  static __host__ __device__ constexpr uint32_t col_p(int b) { return 256u + D + (b ? 64u : 0u); }
+  static __host__ __device__ constexpr uint32_t col_o(int h) { return 256u + h * D; }
+  static __host__ __device__ constexpr uint32_t col_p(int b) {
+    return 256u + kHalves * D + (b ? 64u : 0u);
+  }
+  static_assert(256 + kHalves * D + 128 <= 512, "tensor memory columns");
 };
 
 struct Bars1 {
@@ -87,13 +108,14 @@ struct Bars1 {
   uint64_t pv_done[2];   // P·V(j) done: P[j mod 2] reusable, O holds steps ≤ j (tensor core)
   uint64_t o_free;       // a unit's O has been read out (softmax -> P·V issuer)
   uint64_t mma_done;
+  uint64_t xch[4][2];    // halves: both warps of lanes 32q… posted (m, l) (unit parity)
   uint32_t tmem_base;
   uint32_t abort;
 };
-static_assert(sizeof(Bars1) <= 256, "barrier block");
+static_assert(sizeof(Bars1) <= 512, "barrier block");
 
 template <int D, bool CAUSAL, bool GEN = false>
-__global__ void __launch_bounds__(kThreads1, 1)
+__global__ void __launch_bounds__(Cfg1<D>::kThreads, 1)
     fa_fwd1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                    const FwdParams p) {
@@ -113,8 +135,8 @@ __global__ void __launch_bounds__(kThreads1, 1)
       mbar_init(&bars->q_full[b], 1);
       mbar_init(&bars->q_empty[b], 1);
       mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_free[b], 4);
-      mbar_init(&bars->p_full[b], 4);
+      mbar_init(&bars->s_free[b], C::kSoftWarps);
+      mbar_init(&bars->p_full[b], C::kSoftWarps);
       mbar_init(&bars->pv_done[b], 1);
     }
 #pragma unroll
@@ -123,12 +145,17 @@ __global__ void __launch_bounds__(kThreads1, 1)
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->kv_empty[s], 2);
     }
-    mbar_init(&bars->o_free, 4);
+    mbar_init(&bars->o_free, C::kSoftWarps);
     mbar_init(&bars->mma_done, 2);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&bars->xch[q][0], 2);
+      mbar_init(&bars->xch[q][1], 2);
+    }
     bars->abort = 0u;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == C::kWarpS) {
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
@@ -143,7 +170,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
   const WaitCtl wc{&bars->abort, p.status, p.timeout_ns};
   const WaitCtl drain = drain_ctl(p.timeout_ns);
 
-  if (warp == 5) {
+  if (warp == C::kWarpLoad) {
     // ------------------------------------------------------------ TMA producer
     const bool leader = lane == 0;
     if (leader) {
@@ -174,9 +201,11 @@ __global__ void __launch_bounds__(kThreads1, 1)
       }
       __syncwarp();
       ++qn;
-      int kt = u.kb - 1;
+      UnitSteps<CAUSAL, GEN> us;
+      us.begin(p, u);
       for (int j = 0; j < u.n_steps; ++j, ++g) {
-        kt = next_kt<CAUSAL, GEN>(p, u, kt, 0);  // (dense: kt = j)
+        us.next(u, j);
+        const int kt = us.kt;
         const int st = g % C::kStages;
         const int use = g / C::kStages;
         if (use > 0 && !mbar_wait_warp(&bars->kv_empty[st], (use - 1) & 1, wc)) { ok = false; break; }
@@ -205,7 +234,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
       mbar_wait_warp(&bars->k_full[st], last_use & 1, drain);
       mbar_wait_warp(&bars->v_full[st], last_use & 1, drain);
     }
-  } else if (warp == 4 || warp == 6) {
+  } else if (warp == C::kWarpS || warp == C::kWarpPV) {
     // ------------------------------------------------------------ MMA issuers
     const bool leader = lane == 0;
     auto commit = [&](uint64_t* bar) {
@@ -213,7 +242,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
       __syncwarp();
     };
     bool ok = true;
-    if (warp == 4) {
+    if (warp == C::kWarpS) {
       // S(j) = Q·K(j)ᵀ : M=128, N=128, K=D in steps of 16 (32 bytes inside a 128-byte
       // swizzled row; a new 16 KB box every 64 columns), into S[j mod 2].
       const uint32_t idesc = idesc_bf16(kBlockM, kBlockN, false) | p.s_negate;
@@ -255,9 +284,10 @@ __global__ void __launch_bounds__(kThreads1, 1)
         ++qn;
       }
     } else {
-      // O += P(j)·V(j) : A = P from TMEM (8 columns = 16 keys per step), B = V tile, MN-major
-      // (D contiguous): 16 keys = 2048 bytes per step; next 64-wide column block (leading
-      // byte offset) 16 KB away; next 8-key group (stride byte offset) 1 KB away.
+      // O_h += P_h(j)·V_h(j) : A = P from TMEM (8 columns = 16 keys per step), B = V tile,
+      // MN-major (D contiguous): 16 keys = 2048 bytes per step; next 64-wide column block
+      // (leading byte offset) 16 KB away; next 8-key group (stride byte offset) 1 KB away.
+      // Half h takes the keys 64h … of the tile into its own accumulator.
       const uint32_t idesc = idesc_bf16(kBlockM, D, true);
       const uint32_t v_base = smem_u32(smem + C::kVOff);
       int g = 0, nunits = 0;
@@ -281,10 +311,12 @@ __global__ void __launch_bounds__(kThreads1, 1)
           if (leader) {
             const uint32_t va = v_base + st * C::kTileBytes;
 #pragma unroll
-            for (int kk = 0; kk < kBlockN / 16; ++kk)
-              mma_ts(tmem + C::kColO, tmem + C::col_p(b) + kk * 8,
-                     sdesc_sw128(va + kk * 2048, C::kSubBytes, 1024), idesc,
-                     (j > 0 || kk > 0) ? 1u : 0u);
+            for (int h = 0; h < C::kHalves; ++h)
+#pragma unroll
+              for (int kk = 0; kk < C::kCols / 16; ++kk)
+                mma_ts(tmem + C::col_o(h), tmem + C::col_p(b) + h * (C::kCols / 2) + kk * 8,
+                       sdesc_sw128(va + (h * (C::kCols / 16) + kk) * 2048, C::kSubBytes, 1024),
+                       idesc, (j > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&bars->pv_done[b]);
             mma_commit(&bars->kv_empty[st]);  // V(j) is free once this product is done
           }
@@ -297,18 +329,23 @@ __global__ void __launch_bounds__(kThreads1, 1)
     // Nothing may still be running on the tensor core when TMEM is released.
     commit(&bars->mma_done);
     mbar_wait_warp(&bars->mma_done, 0, drain);
-  } else if (warp < 4) {
+  } else if (warp < C::kSoftWarps) {
     // ------------------------------------------------------------ softmax warps
-    const int row = warp * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_o = tmem + lane_off + C::kColO;
+    constexpr int H = C::kHalves;
+    constexpr int kC = C::kCols;              // keys of a step this warp owns
+    const int quad = warp & 3;                // TMEM lanes 32·quad … (query rows)
+    const int half = warp >> 2;               // keys kC·half … of each step (H = 2)
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t t_o = tmem + lane_off + C::col_o(half);
     const float c = p.scale_log2;
 
-    int g = 0;  // K steps consumed so far over this CTA's units
+    int g = 0;    // K steps consumed so far over this CTA's units
+    int ne = 0;   // epilogues done (unit parity of the halves' exchange)
     bool ok = true;
     // Where a unit's rows go: the bf16 output (row_idx; r0 = the warp's first row, for the
     // TMA store) and LSE, or (general form with several key ranges) the fp32 partial row
-    // and LSE of its range (part_idx).
+    // and LSE of its range (part_idx). With two halves each warp writes half of the columns.
     struct RowOut {
       size_t row_idx, part_idx;
       int r0, bh;
@@ -321,8 +358,10 @@ __global__ void __launch_bounds__(kThreads1, 1)
                         static_cast<size_t>(q_row),
                     r0, bh, q_row < p.T, GEN && p.n_splits > 1};
     };
+    constexpr int kOutCols = D / H;           // output columns this warp writes
+    const int c_out = half * kOutCols;
     auto write_lse = [&](const RowOut& w, float v) {
-      if (!w.in_range) return;
+      if (!w.in_range || half != 0) return;
       if (w.partial) p.lse_part[w.part_idx] = v;
       else p.lse[w.row_idx] = v;
     };
@@ -330,77 +369,146 @@ __global__ void __launch_bounds__(kThreads1, 1)
     auto write_const_row = [&](const RowOut& w, uint32_t bits) {
       if (!w.in_range) return;
       if (w.partial) {
-        float4* prow = reinterpret_cast<float4*>(p.o_part + w.part_idx * D);
+        float4* prow = reinterpret_cast<float4*>(p.o_part + w.part_idx * D + c_out);
         const float f = u2f(bits);
 #pragma unroll
-        for (int t = 0; t < D / 4; ++t) prow[t] = make_float4(f, f, f, f);
+        for (int t = 0; t < kOutCols / 4; ++t) prow[t] = make_float4(f, f, f, f);
       } else {
-        uint4* orow = reinterpret_cast<uint4*>(p.o + w.row_idx * D);
+        uint4* orow = reinterpret_cast<uint4*>(p.o + w.row_idx * D + c_out);
         const uint32_t b2 = pack_bf16x2(u2f(bits), u2f(bits));
 #pragma unroll
-        for (int t = 0; t < D / 8; ++t) orow[t] = make_uint4(b2, b2, b2, b2);
+        for (int t = 0; t < kOutCols / 8; ++t) orow[t] = make_uint4(b2, b2, b2, b2);
       }
     };
     auto fail_rows = [&](const RowOut& w) {
       write_const_row(w, 0x7FC00000u);
       write_lse(w, __uint_as_float(0x7FC00000u));
     };
-    // The finished unit's O (TMEM, after its last P·V) to the output: read 32 columns at a
-    // time, scale by 1/l, stage in this warp's 4 KB slice in the O map's 128-byte-swizzled
-    // layout (16-byte chunk c of row r at c ^ (r mod 8)), one TMA store per 64 columns; rows
-    // past the sequence are not written. O is released to the next unit's first P·V as soon
-    // as it has been read.
-    // (General form: a row that saw no key of the range has l = 0 and gets O = 0, LSE = −∞;
-    // partial rows go out as fp32, each thread writing its own row.)
-    auto epilogue = [&](const RowOut& w, float l, float m) {
-      const float inv_l = (GEN && !(l > 0.0f)) ? 0.0f : 1.0f / l;
-      uint8_t* slice = smem + C::kOOff + warp * 4096;
-      const uint32_t ob = smem_u32(slice) + lane * 128;
-#pragma unroll 1
-      for (int hb = 0; hb < D / 64; ++hb) {
-        uint32_t o[64];
-        tmem_ld32(t_o + hb * 64, o);
-        tmem_ld32(t_o + hb * 64 + 32, o + 32);
-        tmem_ld_wait();
-        reg_fence32(o);
-        reg_fence32(o + 32);
-        if (hb == D / 64 - 1) {
+    // The finished unit's O (TMEM, after its last P·V) to the output; O is released to the
+    // next unit's first P·V as soon as it has been read. (General form: a row that saw no
+    // key of the range has l = 0 and gets O = 0, LSE = −∞; partial rows go out as fp32, each
+    // thread writing its own row.)
+    //
+    // H = 1: read 32 columns at a time, scale by 1/l, stage in this warp's 4 KB slice in the
+    // O map's 128-byte-swizzled layout (16-byte chunk c of row r at c ^ (r mod 8)), one TMA
+    // store per 64 columns; rows past the sequence are not written.
+    //
+    // H = 2: the two warps of a row post their (m, l) in shared memory and meet on an
+    // mbarrier (bounded wait); each then reads its 32 output columns of both accumulators,
+    // merges them with the weights 2^(m_h − m) / l and writes them straight to memory.
+    // Returns false when the meeting gave up (the rows are then written as failed).
+    auto epilogue = [&](const RowOut& w, float l, float m) -> bool {
+      if constexpr (H == 2) {
+        const int par = ne & 1;
+        float2* xs = reinterpret_cast<float2*>(smem + C::kXchOff) + (par * H) * kBlockM;
+        xs[half * kBlockM + row] = make_float2(m, l);
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->xch[quad][par]);
+        const bool met = mbar_wait_warp(&bars->xch[quad][par], (ne >> 1) & 1, wc);
+        ++ne;
+        if (!met) {
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->o_free);
+          fail_rows(w);
+          return false;
         }
-        if (GEN && w.partial) {
-          if (w.in_range) {
-            float4* prow = reinterpret_cast<float4*>(p.o_part + w.part_idx * D + hb * 64);
+        const float2 other = xs[(1 - half) * kBlockM + row];
+        const float m0 = half ? other.x : m, l0 = half ? other.y : l;
+        const float m1 = half ? m : other.x, l1 = half ? l : other.y;
+        const float M = fmaxf(m0, m1);
+        const float f0 = (m0 == -INFINITY) ? 0.0f : ex2_approx(m0 - M);
+        const float f1 = (m1 == -INFINITY) ? 0.0f : ex2_approx(m1 - M);
+        const float L = l0 * f0 + l1 * f1;
+        const float inv_l = (GEN && !(L > 0.0f)) ? 0.0f : 1.0f / L;
+        const float w0 = f0 * inv_l, w1 = f1 * inv_l;
+        uint32_t o0[32], o1[32];
+        tmem_ld32(tmem + lane_off + C::col_o(0) + c_out, o0);
+        tmem_ld32(tmem + lane_off + C::col_o(1) + c_out, o1);
+        tmem_ld_wait();
+        reg_fence32(o0);
+        reg_fence32(o1);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_free);
+        if (w.in_range) {
+          if (w.partial) {
+            float4* prow = reinterpret_cast<float4*>(p.o_part + w.part_idx * D + c_out);
 #pragma unroll
-            for (int t = 0; t < 16; ++t)
-              prow[t] = make_float4(u2f(o[4 * t]) * inv_l, u2f(o[4 * t + 1]) * inv_l,
-                                    u2f(o[4 * t + 2]) * inv_l, u2f(o[4 * t + 3]) * inv_l);
+            for (int t = 0; t < 8; ++t)
+              prow[t] = make_float4(fmaf(u2f(o0[4 * t]), w0, u2f(o1[4 * t]) * w1),
+                                    fmaf(u2f(o0[4 * t + 1]), w0, u2f(o1[4 * t + 1]) * w1),
+                                    fmaf(u2f(o0[4 * t + 2]), w0, u2f(o1[4 * t + 2]) * w1),
+                                    fmaf(u2f(o0[4 * t + 3]), w0, u2f(o1[4 * t + 3]) * w1));
+          } else {
+            uint4* orow = reinterpret_cast<uint4*>(p.o + w.row_idx * D + c_out);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              uint32_t pk4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int x = 8 * t + 2 * e;
+                pk4[e] = pack_bf16x2(fmaf(u2f(o0[x]), w0, u2f(o1[x]) * w1),
+                                     fmaf(u2f(o0[x + 1]), w0, u2f(o1[x + 1]) * w1));
+              }
+              orow[t] = make_uint4(pk4[0], pk4[1], pk4[2], pk4[3]);
+            }
           }
-          continue;
         }
-        if (lane == 0) bulk_wait_group_read0();  // the slice's previous store has read it
-        __syncwarp();
+        write_lse(w, (GEN && !(L > 0.0f)) ? -INFINITY : (M + log2f(L)) * 0.69314718055994530942f);
+        return true;
+      } else {
+        const float inv_l = (GEN && !(l > 0.0f)) ? 0.0f : 1.0f / l;
+        uint8_t* slice = smem + C::kOOff + warp * 4096;
+        const uint32_t ob = smem_u32(slice) + lane * 128;
+#pragma unroll 1
+        for (int hb = 0; hb < D / 64; ++hb) {
+          uint32_t o[64];
+          tmem_ld32(t_o + hb * 64, o);
+          tmem_ld32(t_o + hb * 64 + 32, o + 32);
+          tmem_ld_wait();
+          reg_fence32(o);
+          reg_fence32(o + 32);
+          if (hb == D / 64 - 1) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->o_free);
+          }
+          if (GEN && w.partial) {
+            if (w.in_range) {
+              float4* prow = reinterpret_cast<float4*>(p.o_part + w.part_idx * D + hb * 64);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          st_shared_v4(ob + ((ch ^ (lane & 7)) << 4),
-                       pack_bf16x2(u2f(o[8 * ch]) * inv_l, u2f(o[8 * ch + 1]) * inv_l),
-                       pack_bf16x2(u2f(o[8 * ch + 2]) * inv_l, u2f(o[8 * ch + 3]) * inv_l),
-                       pack_bf16x2(u2f(o[8 * ch + 4]) * inv_l, u2f(o[8 * ch + 5]) * inv_l),
-                       pack_bf16x2(u2f(o[8 * ch + 6]) * inv_l, u2f(o[8 * ch + 7]) * inv_l));
-        fence_proxy_async_smem();  // the staged rows, visible to the TMA engine
-        __syncwarp();
-        if (lane == 0 && w.r0 < p.T) {
-          tma_store_3d(&tm_o, slice, hb * 64, w.r0, w.bh);
-          bulk_commit_group();
+              for (int t = 0; t < 16; ++t)
+                prow[t] = make_float4(u2f(o[4 * t]) * inv_l, u2f(o[4 * t + 1]) * inv_l,
+                                      u2f(o[4 * t + 2]) * inv_l, u2f(o[4 * t + 3]) * inv_l);
+            }
+            continue;
+          }
+          if (lane == 0) bulk_wait_group_read0();  // the slice's previous store has read it
+          __syncwarp();
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            st_shared_v4(ob + ((ch ^ (lane & 7)) << 4),
+                         pack_bf16x2(u2f(o[8 * ch]) * inv_l, u2f(o[8 * ch + 1]) * inv_l),
+                         pack_bf16x2(u2f(o[8 * ch + 2]) * inv_l, u2f(o[8 * ch + 3]) * inv_l),
+                         pack_bf16x2(u2f(o[8 * ch + 4]) * inv_l, u2f(o[8 * ch + 5]) * inv_l),
+                         pack_bf16x2(u2f(o[8 * ch + 6]) * inv_l, u2f(o[8 * ch + 7]) * inv_l));
+          fence_proxy_async_smem();  // the staged rows, visible to the TMA engine
+          __syncwarp();
+          if (lane == 0 && w.r0 < p.T) {
+            tma_store_3d(&tm_o, slice, hb * 64, w.r0, w.bh);
+            bulk_commit_group();
+          }
         }
+        write_lse(w, (GEN && !(l > 0.0f)) ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f);
+        return true;
       }
-      write_lse(w, (GEN && !(l > 0.0f)) ? -INFINITY : (m + log2f(l)) * 0.69314718055994530942f);
     };
     // The pending (finished, not yet written) unit's l, m and output position wait in this
     // thread's 16-byte record in shared memory, not in registers the step loop needs.
     bool pend = false;
-    float4* const prec = reinterpret_cast<float4*>(smem + C::kPendOff) + row;
+    float4* const prec = reinterpret_cast<float4*>(smem + C::kPendOff) + half * kBlockM + row;
     // (.w = bh + BH·split)
     auto parked = [&](float& l, float& m) {
       const float4 v = *prec;
@@ -421,7 +529,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
         tc_fence_after_sync();
         float l, m;
         const RowOut w = parked(l, m);
-        epilogue(w, l, m);
+        if (!epilogue(w, l, m)) ok = false;
         pend = false;
       } else {
         ok = false;
@@ -436,7 +544,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
       const int n = u.nkv[0];
       const int qt = u.qt0;
       const int q_row = qt * kBlockM + row;
-      const RowOut cur = row_out(u.bh, u.split, qt * kBlockM + warp * 32);
+      const RowOut cur = row_out(u.bh, u.split, qt * kBlockM + quad * 32);
       if (!ok) {
         if (pend) fail_pending();
         fail_rows(cur);
@@ -448,38 +556,46 @@ __global__ void __launch_bounds__(kThreads1, 1)
         write_lse(cur, -INFINITY);
         continue;
       }
-      float m_ref = -INFINITY;  // reference max (base-2 scaled units) shared by O and l
+      float m_ref = -INFINITY;  // reference max (base-2 scaled units) shared by O_h and l
       float l = 0.0f;
-      int kt = u.kb - 1;
+      // the tile's K tiles (GEN: its walk, the next position fetched a step ahead)
+      Walk w{nullptr, 0};
+      int nx = 0;
+      if constexpr (GEN) {
+        w = walk_of<CAUSAL>(p, u, 0);
+        nx = walk_next(w, u.kb - 1);
+      }
+      int kt = u.kb - 1;  // (dense: u.kb = 0, step j is K tile j)
       for (int j = 0; j < n; ++j, ++g) {
-        kt = next_kt<CAUSAL, GEN>(p, u, kt, 0);  // (dense: kt = j)
+        if constexpr (GEN) {
+          kt = nx;
+          nx = walk_next(w, kt);
+        } else {
+          ++kt;
+        }
         const int b = g & 1;
         if (!mbar_wait_warp(&bars->s_full[b], (g >> 1) & 1, wc)) { ok = false; break; }
         FA1_TRACE(30, j);
         tc_fence_after_sync();
-        const int k0 = kt * kBlockN;
+        const int k0 = kt * kBlockN + half * kC;
         // Keys past the end of the sequence, and (causal) keys after this query (general
         // form: after query + Tk − Tq).
         int lim;
         bool masked;
         if constexpr (GEN) {
           lim = (CAUSAL ? min(q_row + 1 + p.kv_off, p.Tk) : p.Tk) - k0;
-          masked = lim < kBlockN;
+          masked = lim < kC;
         } else {
           lim = (CAUSAL ? min(q_row + 1, p.T) : p.T) - k0;
-          masked = (CAUSAL && kt == qt) || (k0 + kBlockN > p.T);
+          masked = (CAUSAL && kt == qt) || (k0 + kC > p.T);
         }
-        uint32_t s[kBlockN];
-        const uint32_t t_s = tmem + lane_off + C::col_s(b);
-        tmem_ld32(t_s + 0, s);
-        tmem_ld32(t_s + 32, s + 32);
-        tmem_ld32(t_s + 64, s + 64);
-        tmem_ld32(t_s + 96, s + 96);
+        uint32_t s[kC];
+        const uint32_t t_s = tmem + lane_off + C::col_s(b) + half * kC;
+#pragma unroll
+        for (int c0 = 0; c0 < kC; c0 += 32) tmem_ld32(t_s + c0, s + c0);
         tmem_ld_wait();
-        reg_fence32(s);
-        reg_fence32(s + 32);
-        reg_fence32(s + 64);
-        reg_fence32(s + 96);
+#pragma unroll
+        for (int c0 = 0; c0 < kC; c0 += 32) reg_fence32(s + c0);
         // S(g) is in registers: the tensor core may compute S(g + 2) into this region.
         tc_fence_before_sync();
         __syncwarp();
@@ -487,14 +603,14 @@ __global__ void __launch_bounds__(kThreads1, 1)
         FA1_TRACE(20, j);
         if (masked) {
 #pragma unroll
-          for (int t = 0; t < kBlockN; ++t)
+          for (int t = 0; t < kC; ++t)
             if (t >= lim) s[t] = __float_as_uint(-INFINITY);
         }
         float mx[8];
 #pragma unroll
         for (int a = 0; a < 8; ++a) mx[a] = fmaxf(u2f(s[2 * a]), u2f(s[2 * a + 1]));
 #pragma unroll
-        for (int t = 16; t < kBlockN; t += 16)
+        for (int t = 16; t < kC; t += 16)
 #pragma unroll
           for (int a = 0; a < 8; ++a) mx[a] = fmax3(mx[a], u2f(s[t + 2 * a]), u2f(s[t + 2 * a + 1]));
         const float m_tile =
@@ -513,15 +629,16 @@ __global__ void __launch_bounds__(kThreads1, 1)
         const bool any_rescale = __any_sync(0xffffffffu, rescale);
         FA1_TRACE(40, j);
 
-        // p = 2^(s·c − m_ref) on fp32 pairs; row sum in fp32; P kept as bf16 pairs. (General
-        // form: a row that has seen no key yet has m_ref = −∞ and all its p are 0.)
+        // p = 2^(s·c − m_ref) on fp32 pairs; row sum in fp32; P kept as bf16 pairs. (A row
+        // whose keys so far are all masked — the general form, or a half at the causal
+        // diagonal — has m_ref = −∞ and all its p are 0.)
         const uint64_t c2 = f2_pack(c, c);
-        const float m_use = (GEN && m_ref == -INFINITY) ? 0.0f : m_ref;
+        const float m_use = ((GEN || H == 2) && m_ref == -INFINITY) ? 0.0f : m_ref;
         const uint64_t nm2 = f2_pack(-m_use, -m_use);
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-        uint32_t pk[kBlockN / 2];
+        uint32_t pk[kC / 2];
 #pragma unroll
-        for (int t = 0; t < kBlockN / 2; ++t) {
+        for (int t = 0; t < kC / 2; ++t) {
           const uint64_t x2 = f2_fma(f2_pack(u2f(s[2 * t]), u2f(s[2 * t + 1])), c2, nm2);
           float x0, x1;
           f2_unpack(x2, x0, x1);
@@ -533,9 +650,9 @@ __global__ void __launch_bounds__(kThreads1, 1)
         }
         FA1_TRACE(42, j);
         if (any_rescale) {
-          // Rows whose max jumped bring O to the new reference before this step's P·V (rare:
-          // the reference moves only by more than τ). O must hold every earlier step: the
-          // previous P·V done (j ≥ 1, so it belongs to this unit).
+          // Rows whose max jumped bring their O_h to the new reference before this step's
+          // P·V (rare: the reference moves only by more than τ). O_h must hold every earlier
+          // step: the previous P·V done (j ≥ 1, so it belongs to this unit).
           if (!mbar_wait_warp(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, wc)) { ok = false; break; }
           tc_fence_after_sync();
 #pragma unroll
@@ -555,9 +672,9 @@ __global__ void __launch_bounds__(kThreads1, 1)
           tc_fence_after_sync();
         }
         FA1_TRACE(44, j);
-        const uint32_t t_p = tmem + lane_off + C::col_p(b);
-        tmem_st32(t_p, pk);
-        tmem_st32(t_p + 32, pk + 32);
+        const uint32_t t_p = tmem + lane_off + C::col_p(b) + half * (kC / 2);
+#pragma unroll
+        for (int c0 = 0; c0 < kC / 2; c0 += 32) tmem_st32(t_p + c0, pk + c0);
         tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
@@ -577,8 +694,11 @@ __global__ void __launch_bounds__(kThreads1, 1)
             tc_fence_after_sync();
             float pl, pm;
             const RowOut w = parked(pl, pm);
-            epilogue(w, pl, pm);
             pend = false;
+            if (!epilogue(w, pl, pm)) {
+              ok = false;
+              break;
+            }
           } else {
             ok = false;
             break;
@@ -601,7 +721,7 @@ __global__ void __launch_bounds__(kThreads1, 1)
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == C::kWarpS) {
     __syncwarp();
     tc_fence_after_sync();
     tmem_dealloc(tmem, 512);

@@ -192,14 +192,33 @@ __device__ __forceinline__ int unit_index(int round, int cta, int grid) {
   return round * grid + ((round & 1) ? grid - 1 - cta : cta);
 }
 
+// General form: the K tiles of a unit's range that Q tile i uses, walked by a cursor over
+// the tile's block-mask row. The cursor keeps two values (the row, the end of the tile's
+// visible keys) instead of the unit, and callers fetch the next position a step ahead of
+// its use, so the mask byte's load is not on the step's critical path.
+struct Walk {
+  const uint8_t* mrow;  // block-mask row of the tile (nullptr: every K tile)
+  int end;              // past the last K tile the tile may use (range end, causal limit)
+};
+constexpr int kNoTile = 0x7fffffff;
+
 template <bool CAUSAL>
-__device__ __forceinline__ bool gen_active(const FwdParams& p, const Unit& u, int i, int kt) {
+__device__ __forceinline__ Walk walk_of(const FwdParams& p, const Unit& u, int i) {
+  // (ternaries, not u.last[i]: a runtime index would move the unit to local memory)
   const int qt = u.qt0 + i;
-  if (i >= p.tiles_per_cta || qt * kBlockM >= p.T) return false;
-  if (CAUSAL && kt > (i ? u.last[1] : u.last[0])) return false;
-  if (p.bmask != nullptr)
-    return p.bmask[(static_cast<size_t>(u.mh) * p.n_qt + qt) * p.n_kv + kt] != 0;
-  return true;
+  const bool exists = i < p.tiles_per_cta && qt * kBlockM < p.T;
+  const int last = i ? u.last[1] : u.last[0];
+  Walk w;
+  w.end = !exists ? u.kb : (CAUSAL ? min(u.ke, last + 1) : u.ke);
+  w.mrow = p.bmask ? p.bmask + (static_cast<size_t>(u.mh) * p.n_qt + qt) * p.n_kv : nullptr;
+  return w;
+}
+
+// The first K tile after kt that the walk uses, kNoTile when none is left.
+__device__ __forceinline__ int walk_next(const Walk& w, int kt) {
+  for (++kt; kt < w.end; ++kt)
+    if (w.mrow == nullptr || w.mrow[kt] != 0) return kt;
+  return kNoTile;
 }
 
 template <bool CAUSAL, bool GEN>
@@ -220,14 +239,22 @@ __device__ __forceinline__ Unit unit_of(const FwdParams& p, int L) {
     for (int i = 0; i < 2; ++i) {
       const int last_row = min((u.qt0 + i) * kBlockM + kBlockM - 1, p.T - 1);
       u.last[i] = CAUSAL ? min(p.n_kv - 1, (last_row + p.kv_off) / kBlockN) : p.n_kv - 1;
-      u.nkv[i] = 0;
     }
-    u.n_steps = 0;
-    for (int kt = u.kb; kt < u.ke; ++kt) {
-      const bool a0 = gen_active<CAUSAL>(p, u, 0, kt), a1 = gen_active<CAUSAL>(p, u, 1, kt);
-      u.nkv[0] += a0;
-      u.nkv[1] += a1;
-      u.n_steps += (a0 || a1);
+    const Walk w0 = walk_of<CAUSAL>(p, u, 0), w1 = walk_of<CAUSAL>(p, u, 1);
+    if (p.bmask == nullptr) {  // every K tile of [kb, end_i): contiguous
+      u.nkv[0] = max(0, w0.end - u.kb);
+      u.nkv[1] = max(0, w1.end - u.kb);
+      u.n_steps = max(u.nkv[0], u.nkv[1]);
+    } else {
+      u.nkv[0] = u.nkv[1] = u.n_steps = 0;
+      const int hi = max(w0.end, w1.end);
+      for (int kt = u.kb; kt < hi; ++kt) {
+        const bool a0 = kt < w0.end && w0.mrow[kt] != 0;
+        const bool a1 = kt < w1.end && w1.mrow[kt] != 0;
+        u.nkv[0] += a0;
+        u.nkv[1] += a1;
+        u.n_steps += (a0 || a1);
+      }
     }
     return u;
   }
@@ -249,27 +276,41 @@ __device__ __forceinline__ Unit unit_of(const FwdParams& p, int L) {
   return u;
 }
 
-// Step → K tile. Dense: step j is K tile j and tile i is active while j < nkv[i]. GEN: the
-// cursor kt advances to the next K tile that the tile (i ≥ 0) or any tile (i < 0) uses.
+// General form: the steps of a unit for a role that follows both tiles (producer, MMA
+// issuers). Step j is K tile kt, the smaller of the two tiles' next K tiles, and tile i takes
+// part when act[i]. (Dense units need none of this: step j is K tile j, and tile i is active
+// while j < nkv[i].)
 template <bool CAUSAL, bool GEN>
-__device__ __forceinline__ int next_kt(const FwdParams& p, const Unit& u, int kt, int i) {
-  if constexpr (!GEN) {
-    return kt + 1;
-  } else {
-    for (++kt; kt < u.ke; ++kt) {
-      const bool a = (i >= 0) ? gen_active<CAUSAL>(p, u, i, kt)
-                              : (gen_active<CAUSAL>(p, u, 0, kt) || gen_active<CAUSAL>(p, u, 1, kt));
-      if (a) break;
+struct UnitSteps {
+  Walk w[2];
+  int nx[2];
+  int kt;
+  bool act[2];
+  __device__ __forceinline__ void begin(const FwdParams& p, const Unit& u) {
+    kt = -1;
+    if constexpr (GEN) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        w[i] = walk_of<CAUSAL>(p, u, i);
+        nx[i] = walk_next(w[i], u.kb - 1);
+      }
     }
-    return kt;
   }
-}
-
-template <bool CAUSAL, bool GEN>
-__device__ __forceinline__ bool tile_active(const FwdParams& p, const Unit& u, int i, int kt, int j) {
-  if constexpr (!GEN) return j < u.nkv[i];
-  else return gen_active<CAUSAL>(p, u, i, kt);
-}
+  __device__ __forceinline__ void next(const Unit& u, int j) {
+    if constexpr (GEN) {
+      kt = min(nx[0], nx[1]);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        act[i] = nx[i] == kt;
+        if (act[i]) nx[i] = walk_next(w[i], kt);  // (the next position, a step ahead)
+      }
+    } else {
+      kt = j;
+      act[0] = j < u.nkv[0];
+      act[1] = j < u.nkv[1];
+    }
+  }
+};
 
 // QK8: Q and K arrive as e4m3 codes (their per-tensor scales folded into scale_log2) and
 // S = Q·Kᵀ runs as a kind::f8f6f4 product; V, P and O are as in the bf16 path.
@@ -366,9 +407,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       ++qn;
+      UnitSteps<CAUSAL, GEN> us;
+      if constexpr (GEN) us.begin(p, u);
       int kt = u.kb - 1;
       for (int j = 0; j < u.n_steps; ++j, ++g) {
-        kt = next_kt<CAUSAL, GEN>(p, u, kt, -1);
+        if constexpr (GEN) {
+          us.next(u, j);
+          kt = us.kt;
+        } else {
+          ++kt;
+        }
         const int st = g % C::kStages;
         const int use = g / C::kStages;
         if (use > 0 && !mbar_wait_warp(&bars->kv_empty[st], (use - 1) & 1, wc)) { ok = false; break; }
@@ -449,15 +497,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit u = unit_of<CAUSAL, GEN>(p, L);
         const int qb = qn % C::kQBufs;
         if (!mbar_wait_warp(&bars->q_full[qb], (qn / C::kQBufs) & 1, wc)) { ok = false; break; }
-        int kt = u.kb - 1;
+        UnitSteps<CAUSAL, GEN> us;
+        if constexpr (GEN) us.begin(p, u);
         for (int j = 0; j < u.n_steps; ++j, ++g) {
-          kt = next_kt<CAUSAL, GEN>(p, u, kt, -1);
+          if constexpr (GEN) us.next(u, j);
           const int st = g % C::kStages;
           if (!mbar_wait_warp(&bars->k_full[st], (g / C::kStages) & 1, wc)) { ok = false; break; }
           tc_fence_after_sync();
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            if (!tile_active<CAUSAL, GEN>(p, u, i, kt, j)) continue;
+            if (GEN ? !us.act[i] : j >= u.nkv[i]) continue;
             if (ns[i] > 0) {
               // S_i may be overwritten once its softmax has read it (P in its own columns)
               // or, when P_i lives in S_i's columns, once P_i·V has consumed P_i.
@@ -507,15 +556,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int L = unit_index(r, cta, grid);
         if (L >= p.total_units) continue;
         const Unit u = unit_of<CAUSAL, GEN>(p, L);
-        int kt = u.kb - 1;
+        UnitSteps<CAUSAL, GEN> us;
+        if constexpr (GEN) us.begin(p, u);
         int jt[2] = {0, 0};   // steps of this unit in which tile i was active
         for (int j = 0; j < u.n_steps; ++j, ++g) {
-          kt = next_kt<CAUSAL, GEN>(p, u, kt, -1);
+          if constexpr (GEN) us.next(u, j);
           const int st = g % C::kStages;
           if (!mbar_wait_warp(&bars->v_full[st], (g / C::kStages) & 1, wc)) { ok = false; break; }
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            if (!tile_active<CAUSAL, GEN>(p, u, i, kt, j)) continue;
+            if (GEN ? !us.act[i] : j >= u.nkv[i]) continue;
             if (jt[i] == 0 && nunits[i] > 0) {
               // This unit's first P·V overwrites O_i: the previous unit's O_i must have
               // been read out.
@@ -733,9 +783,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       float m_ref = -INFINITY;  // reference max (base-2 scaled units) shared by O and l
       float l = 0.0f;
-      int kt = u.kb - 1;
+      // this tile's K tiles (GEN: its walk, the next position fetched a step ahead)
+      Walk w{nullptr, 0};
+      int nx = 0;
+      if constexpr (GEN) {
+        w = walk_of<CAUSAL>(p, u, wg);
+        nx = walk_next(w, u.kb - 1);
+      }
+      int kt = u.kb - 1;  // (dense: u.kb = 0, step j is K tile j)
       for (int j = 0; j < n; ++j, ++gs) {
-        kt = next_kt<CAUSAL, GEN>(p, u, kt, wg);
+        if constexpr (GEN) {
+          kt = nx;
+          nx = walk_next(w, kt);
+        } else {
+          ++kt;
+        }
         if (!mbar_wait_warp(&bars->s_full[wg], gs & 1, wc)) { ok = false; break; }
         FA_TRACE(30 + wg, j);
         tc_fence_after_sync();
