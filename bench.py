@@ -19,6 +19,7 @@ L2: each step touches ~0.8 GB of distinct inputs and outputs (more than 6× the 
 so every launch reads inputs last touched a full step earlier.
 
 The same line carries `decode` (one query per head against a 16k-token KV cache, GB/s),
+`fwd_kv_few_queries` (2, 8 and 128 new queries per head against the same cache, GB/s),
 `block_sparse` (T = 8192 with half the 128×128 blocks kept, TFLOP/s on kept blocks),
 `fp8_qk` (e4m3 queries and keys, bf16 values, B2 H16 T16384 d128, causal), `fwd_cta_pair`
 (the T = 16384 launch on CTA pairs that share each tensor-core product, beside the default
@@ -551,6 +552,36 @@ def _general_forms(args, fa, inputs, torch, dev, stream, bf16_peak, hbm_peak, ws
                                "fa_fwd_combine_kernel; achieved over the whole fa_fwd_kv call; "
                                "traffic of the decode kernel"},
         "gpu_launches": 2 * args.steps,
+    }
+    # a few new queries per head against the same cache (speculative decoding, chunked
+    # prefill): Tq = 2 on the CUDA-core multi-query kernel, 8 and 128 on the one-tile
+    # tensor-core kernel; the same bytes as decode, HBM-bound
+    few = {}
+    for tq in (2, 8, 128):
+        qm = q[:, :, -tq:].contiguous()
+        om = torch.empty_like(qm)
+        lm = torch.empty((B, H, tq), dtype=torch.float32, device=dev)
+        need_m = fa.fa_fwd_kv_workspace_size(B, H, tq, DECODE_TK, D, 0)
+        wsm = torch.empty(max(need_m, 1), dtype=torch.uint8, device=dev)
+
+        def few_call():
+            rc = fa.fa_fwd_kv(qm.data_ptr(), k.data_ptr(), v.data_ptr(), om.data_ptr(),
+                              lm.data_ptr(), B, H, tq, DECODE_TK, D, 1, scale, 0, wsm.data_ptr(),
+                              wsm.numel(), stream.cuda_stream)
+            if rc != fa.FA_OK:
+                raise fa.FAError(rc, "fa_fwd_kv")
+        ms_m = _time_calls(few_call, args.steps, args.warmup, stream, torch, ws)
+        byts_m = 2.0 * B * H * DECODE_TK * D * 2 + B * H * tq * D * 2 * 2 + B * H * tq * 4
+        few[f"tq{tq}"] = {"us_per_call": ms_m * 1e3, "GB/s": ws * byts_m / ms_m / 1e6,
+                          "frac_of_hbm": byts_m / ms_m / 1e6 / hbm_peak}
+        del qm, om, lm, wsm
+    out["fwd_kv_few_queries"] = {
+        "metric": "fa_fwd_kv GB/s (bf16, B4 H12 d64, Tq new queries vs 16384 cached keys, causal)",
+        "unit": "GB/s", "steps": args.steps, **few,
+        "kernel": "Tq = 2: fa_decode_multi_kernel<64,2> (CUDA cores); Tq = 8, 128: "
+                  "fa_fwd1_kernel<64,causal,general> (one Q tile per unit, key ranges) + "
+                  "fa_fwd_combine_kernel",
+        "gpu_launches": 2 * 3 * args.steps,
     }
     del q, k, v, qd, o, lse, wsb
     # block-sparse: tensor-bound on the kept blocks

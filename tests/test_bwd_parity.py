@@ -15,8 +15,10 @@ rounding of G adds ≤ u·|G|. The bound doubles the first term's constant; repl
 kernel's roundings in fp64 on these workloads reaches at most 0.65 of u·M_G. The last term
 covers fp32 noise where the exact gradient is 0 (causal query 0: dQ_0 = 0).
 
-Sampled full-size checks (T = 4096, 16384), where the magnitudes would cost a full
-backward on the CPU, use scale-relative bounds instead:
+Whole heads of the full-size launches (T = 16384 at d = 64, T = 8192 at d = 128) are
+checked element by element under that bound, the oracle computing the magnitudes of those
+heads alone. Sampled checks across the other heads (T = 4096, 16384), where the magnitudes
+of every head would cost a full backward on the CPU, use scale-relative bounds instead:
     max|G − G_ref| ≤ 2e-2·max|G_ref|,   mean|G − G_ref| ≤ 5e-3·mean|G_ref|
 (the replay above gives at most 5.7e-3 and 2.3e-3 for these ratios at T ≥ 256). A dropped
 term, a wrong mask or a transposed operand gives errors of order 1 under either bound."""
@@ -143,6 +145,33 @@ def _sampled_check(w, heads=2):
         idx = torch.from_numpy(rows).cuda()
         got = tuple(t[b, h][idx].float().cpu().double().numpy() for t in (dq, dk, dv))
         _compare_relative(got, (dq_ref, dk_ref, dv_ref), f"{w.name} bh={bh}")
+
+
+@pytest.mark.parametrize("name,causal,bh", [
+    ("sweep_t16384", True, 47),
+    ("bwd_d128_t8192", False, 0),
+])
+def test_bwd_parity_whole_head_full_size(name, causal, bh):
+    """One whole head of a full-size launch (every row of dQ, dK and dV) under the
+    element-wise bound of the small workloads, with the oracle's magnitudes for that head:
+    the d = 64 causal sweep at T = 16384 (its last (batch, head)) and the d = 128
+    non-causal T = 8192 workload (its first)."""
+    torch = _torch()
+    import exact_attention_23_gb300 as fa
+    w = (inputs.WORKLOADS[name] if name in inputs.WORKLOADS
+         else inputs.Workload(name, 2, 8, 8192, 128, causal, 32)).with_causal(causal)
+    q, k, v = inputs.workload_qkv(w)
+    do = inputs.workload_do(w)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.fwd(qd, kd, vd, causal=w.causal)
+    dq, dk, dv = fa.bwd(qd, kd, vd, o, lse, dod, causal=w.causal)
+    torch.cuda.synchronize()
+    b, h = divmod(bh, w.H)
+    got = tuple(t[b:b + 1, h:h + 1].float().cpu().double().numpy() for t in (dq, dk, dv))
+    args = [inputs.to_f64_numpy(t[b:b + 1, h:h + 1]) for t in (q, k, v, do)]
+    ref = oracle.attention_backward(*args, w.causal, w.scale)
+    mags = oracle.attention_backward_magnitudes(*args, w.causal, w.scale)
+    _compare_elementwise(got, ref, mags, f"{w.name} bh={bh} (whole head)")
 
 
 @pytest.mark.parametrize("T", [4096, 16384])

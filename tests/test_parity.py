@@ -190,6 +190,31 @@ def test_parity_wide_head_t16k_sampled(causal):
     _sampled_check(inputs.WORKLOADS["wide_head_t16k"].with_causal(causal))
 
 
+@pytest.mark.parametrize("name,causal", [
+    ("sweep_t16384", True),
+    ("wide_head_t16k", True),
+    ("wide_head_t16k", False),
+])
+def test_parity_whole_heads_t16k(name, causal):
+    """Every row of two whole heads (the first and the last (batch, head) of the launch) at
+    the full 16384-row size, against the oracle's full attention of those heads: each
+    tile position, both ends of the zig-zag unit order and every K step of the last
+    tiles, under the same element-wise tolerances as the small workloads."""
+    torch = _torch()
+    import exact_attention_23_gb300 as fa
+    w = inputs.WORKLOADS[name].with_causal(causal)
+    q, k, v = inputs.workload_qkv(w)
+    o, lse = fa.fwd(q.cuda(), k.cuda(), v.cuda(), causal=w.causal)
+    torch.cuda.synchronize()
+    for bh in (0, w.B * w.H - 1):
+        b, h = divmod(bh, w.H)
+        o_ref, lse_ref = oracle.attention(
+            *(inputs.to_f64_numpy(t[b:b + 1, h:h + 1]) for t in (q, k, v)), w.causal, w.scale)
+        og = o[b:b + 1, h:h + 1].float().cpu().double().numpy()
+        lg = lse[b:b + 1, h:h + 1].cpu().double().numpy()
+        _compare(og, lg, o_ref, lse_ref, f"{w.name} causal={causal} bh={bh} (all rows)")
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_causal_row0_bit_exact_and_lse(d):
     torch = _torch()
