@@ -379,6 +379,16 @@ CONTEXT = {
 }
 
 
+def _fwd_kernel_name(T, torch):
+    """The forward kernel fa_fwd runs at B, H, T, d = 64, causal: pairs of Q tiles when they
+    fill the SMs, else one tile per CTA (the library's short-grid rule)."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    n_pairs = (-(-T // 128) + 1) // 2
+    if n_pairs * B * H < sms:
+        return "fa_fwd1_kernel<64,causal> (one Q tile per CTA)"
+    return "fa_fwd_kernel<64,causal>"
+
+
 def _time_calls(fn, steps, warmup, stream, torch, ws):
     for _ in range(warmup):
         fn()
@@ -901,7 +911,7 @@ def run_gpu(args):
                          "traffic": args.traffic if args.traffic is not None else (
                              _measured_traffic() if dom["T"] == 16384 else None),
                          "algorithmic_bytes": fa.hbm_bytes(B, H, dom["T"], D),
-                         "kernel": f"fa_fwd_kernel<64,causal> at T={dom['T']} "
+                         "kernel": f"{_fwd_kernel_name(dom['T'], torch)} at T={dom['T']} "
                                    f"({fa.flops(B, H, dom['T'], D, True):.4g} FLOP per launch; "
                                    f"peak = {peak_kind} burst bf16)"},
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
