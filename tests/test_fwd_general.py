@@ -174,6 +174,28 @@ def test_fwd_kv_prefill_many_units_per_cta_d128():
                      f"kv prefill d128 head ({b},{h}) row {r}")
 
 
+@pytest.mark.parametrize("d,causal", [(64, True), (128, False)])
+def test_fwd_kv_pairs_with_split_ranges(d, causal):
+    """B4 H12, 512 new queries against 16384 cached keys, automatic ranges: on a 152-SM GB300
+    the cost rule picks 3 key ranges, and the 48 · 2 · 3 = 288 pair units fill the SMs, so the
+    pair kernel's general form runs with split ranges (fp32 partial rows, then the merge).
+    Every row of three heads against the oracle."""
+    import torch
+    import exact_attention_23_gb300 as fa
+    B, H, Tq, Tk = 4, 12, 512, 16384
+    assert fa.fa_fwd_kv_workspace_size(B, H, Tq, Tk, d, 0) > 0, "expected split key ranges"
+    q, k, v = _qkv_kv(B, H, Tq, Tk, d, 760 + d)
+    o, lse = fa.fwd_kv(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+    torch.cuda.synchronize()
+    o = o.float().cpu().double().numpy()
+    lse = lse.cpu().double().numpy()
+    for b, h in ((0, 0), (2, 7), (3, 11)):
+        o_ref, lse_ref = oracle.attention_general_head(
+            *(inputs.to_f64_numpy(t[b, h]) for t in (q, k, v)), causal, d ** -0.5)
+        _compare(o[b, h], lse[b, h], o_ref, lse_ref,
+                 f"kv pairs+ranges d{d} causal={causal} head ({b},{h})")
+
+
 def test_fwd_block_sparse_full_and_causal_masks():
     """An all-ones mask is plain attention; keeping the blocks on and below the diagonal
     under causal is plain causal attention (the skipped blocks were fully masked)."""
