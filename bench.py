@@ -395,14 +395,20 @@ def _exp2_rate(torch, dev, dom, clocks):
                     "half of each diagonal tile, which this count leaves out"}
 
 
-def _fwd_kernel_name(T, torch):
-    """The forward kernel fa_fwd runs at B, H, T, d = 64, causal: pairs of Q tiles when they
-    fill the SMs, else one tile per CTA (the library's short-grid rule)."""
+def _fwd_kernel_name_for(b, h, T, torch):
+    """The bf16 forward kernel fa_fwd runs for b·h heads of length T: pairs of Q tiles when
+    they fill the SMs, else one tile per CTA (the library's short-grid rule)."""
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     n_pairs = (-(-T // 128) + 1) // 2
-    if n_pairs * B * H < sms:
-        return "fa_fwd1_kernel<64,causal> (one Q tile per CTA)"
-    return "fa_fwd_kernel<64,causal>"
+    if n_pairs * b * h < sms:
+        return "fa_fwd1_kernel (one Q tile per CTA)"
+    return "fa_fwd_kernel (pairs of Q tiles)"
+
+
+def _fwd_kernel_name(T, torch):
+    """The forward kernel of the sweep's B, H at length T (d = 64, causal)."""
+    name = _fwd_kernel_name_for(B, H, T, torch)
+    return name.replace("_kernel", "_kernel<64,causal>", 1)
 
 
 def _time_calls(fn, steps, warmup, stream, torch, ws):
@@ -687,10 +693,42 @@ def _time_rotating(torch, stream, sets, launch, steps):
     return a.elapsed_time(b) / (reps * n), n
 
 
+# The small named configurations of the test workloads (tiny, ragged, spiky values), each
+# as (workload name, causal).
+SMALL_CONFIGS = (("tiny_causal", True), ("ragged_t1000", True), ("ragged_t1000", False),
+                 ("gpt2_layer_spiky", True))
+
+
+def _small_configs(args, fa, inputs, torch, dev, stream, bf16_peak, hbm_peak):
+    """The forward on each small configuration, W warm-up and K timed launches in turn on
+    the same inputs (the largest is 25 MB of q, k, v, o: L2-resident after the first)."""
+    out = {}
+    for name, causal in SMALL_CONFIGS:
+        w = inputs.WORKLOADS[name].with_causal(causal)
+        q, k, v = (t.to(dev) for t in inputs.workload_qkv(w))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
+
+        def call():
+            rc = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           w.B, w.H, w.T, w.d, int(causal), w.scale, stream.cuda_stream)
+            if rc != fa.FA_OK:
+                raise fa.FAError(rc, "fa_fwd")
+        ms = _time_calls(call, args.steps, args.warmup, stream, torch, 1)
+        fl = fa.flops(w.B, w.H, w.T, w.d, causal)
+        by = fa.hbm_bytes(w.B, w.H, w.T, w.d)
+        out[f"{name}{'' if causal else '_noncausal'}"] = {
+            "shape": f"B{w.B} H{w.H} T{w.T} d{w.d}", "causal": causal, "us_per_call": ms * 1e3,
+            "tflops": fl / ms / 1e9, "frac_of_burst": fl / ms / 1e9 / bf16_peak,
+            "gbs": by / ms / 1e6, "frac_hbm": by / ms / 1e6 / hbm_peak,
+            "kernel": _fwd_kernel_name_for(w.B, w.H, w.T, torch)}
+    return out
+
+
 def run_only(args):
     """One object of the line alone: with --warmup W and --steps K its launches run in a
-    fixed order (for fwd_d128: W + K causal, then W + K non-causal), so a profiler can pick
-    one by its index."""
+    fixed order (fwd_d128: W + K causal, then W + K non-causal; small_configs: W + K of each
+    entry of SMALL_CONFIGS in turn), so a profiler can pick one by its index."""
     import torch
 
     import exact_attention_23_gb300 as fa
@@ -698,8 +736,11 @@ def run_only(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
-    bf16_peak, _, _, _ = _peaks()
-    out = _fwd_d128(args, fa, inputs, torch, dev, stream, bf16_peak, 1)
+    bf16_peak, _, hbm_peak, _ = _peaks()
+    if args.only == "small_configs":
+        out = _small_configs(args, fa, inputs, torch, dev, stream, bf16_peak, hbm_peak)
+    else:
+        out = _fwd_d128(args, fa, inputs, torch, dev, stream, bf16_peak, 1)
     print(json.dumps({"only": args.only, **out}), flush=True)
     return 0
 
@@ -977,7 +1018,7 @@ def main():
     ap.add_argument("--T", type=int, default=0, help="time one length instead of the sweep")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=("fwd_d128",), default=None,
+    ap.add_argument("--only", choices=("fwd_d128", "small_configs"), default=None,
                     help="run one object alone (for a profiler capture) and print it")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
