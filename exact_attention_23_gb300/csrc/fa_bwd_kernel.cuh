@@ -26,7 +26,8 @@
 //   warps 0 .. 4·kCWG−1   compute: warpgroup g owns query columns 32·g .. 32·g+31 of each
 //                         tile (thread = key row); no exchange between warpgroups is needed,
 //                         since P comes from the saved LSE, column by column
-//   next 4 warps          dQ drain: TMEM → registers → vector fp32 atomic adds
+//   next 4 warps          dQ drain: TMEM → registers → shared memory → bulk reduce-adds
+//                         into the fp32 accumulator by the TMA engine
 //   next warp             score issuer: Sᵀ and dPᵀ MMAs (one elected thread); TMEM owner
 //   next warp             gradient issuer: dV, dK and dQ MMAs (one elected thread)
 //   last warp             TMA producer
@@ -87,7 +88,11 @@ struct BwdCfg {
   static constexpr int kDSBytes = 128 * kBQ * 2;      // [128 keys][kBQ queries] bf16, 64-col boxes
   static constexpr int kVecBytes = 2 * kBQ * 4;       // per stage: lse2[kBQ] then D[kBQ]
   static constexpr int kVec = kDS + 2 * kDSBytes;
-  static constexpr int kBar = kVec + kStages * kVecBytes;
+  // Each dQ drain warp stages 16 of its TMEM columns for its 32 lanes (2 KB) for a bulk
+  // reduce-add, two buffers per warp.
+  static constexpr int kDQChunk = 32 * 16 * 4;
+  static constexpr int kDQStage = kVec + kStages * kVecBytes;
+  static constexpr int kBar = kDQStage + 4 * 2 * kDQChunk;
   static constexpr int kSmemBytes = kBar + 256 + 1024;  // barriers + 1 KB alignment slack
   // Tensor memory: Sᵀ, dPᵀ (kBQ columns each), dV, dK (D each), dQ (D columns at d = 64,
   // dQᵀ with kBQ columns at d = 128), Pᵀ as bf16 pairs (kBQ/2 columns).
@@ -140,10 +145,13 @@ struct BwdParams {
 
 constexpr uint32_t kBwdFlagStarveQ = 1u;  // FA_FLAG_TEST_STARVE_Q
 
-// dQ accumulator layouts, chosen so that a warp's 32 vector adds cover 512 contiguous bytes.
-// d = 64 (thread = query row r of a 128-row tile): [bh][tile][d/4][128 rows][4 columns];
-//   dq_acc_offset(bh, i, n_qt, c4, r, d) is query row r, columns 4·c4 .. 4·c4+3.
-// d = 128 (dQᵀ: thread = head dim c of a 64-query tile): [bh][tile][16][128 dims][4 rows];
+// dQ accumulator layouts.
+// d = 64 (thread = query row r of a 128-row tile): [bh][tile][r/32][d/4][32 rows][4 columns],
+//   so the 32 rows of one drain warp and 16 consecutive columns are 2 KB in one piece (one
+//   bulk reduce-add); dq_acc_offset(bh, i, n_qt, c4, r, d) is query row r, columns
+//   4·c4 .. 4·c4+3.
+// d = 128 (dQᵀ: thread = head dim c of a 64-query tile): [bh][tile][c/32][16][32 dims][4 rows],
+//   so the 32 dims of one drain warp and 16 consecutive query rows are 2 KB in one piece;
 //   dq_acc_offset_t(bh, i, n_qt, g, c) is head dim c of query rows 4·g .. 4·g+3.
 // N consecutive TMEM columns (N = 16 or a multiple of 32) of the warp's 32 lanes into r,
 // with one wait for all of them.
@@ -164,10 +172,12 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t* r) {
 
 __host__ __device__ __forceinline__ size_t dq_acc_offset(int bh, int i, int n_qt, int c4, int r,
                                                          int d) {
-  return ((((size_t)bh * n_qt + i) * (size_t)(d / 4) + c4) * 128u + r) * 4u;
+  return (((((size_t)bh * n_qt + i) * 4u + (unsigned)(r >> 5)) * (size_t)(d / 4) + c4) * 32u +
+          (unsigned)(r & 31)) * 4u;
 }
 __host__ __device__ __forceinline__ size_t dq_acc_offset_t(int bh, int i, int n_qt, int g, int c) {
-  return ((((size_t)bh * n_qt + i) * 16u + g) * 128u + c) * 4u;
+  return (((((size_t)bh * n_qt + i) * 4u + (unsigned)(c >> 5)) * 16u + g) * 32u +
+          (unsigned)(c & 31)) * 4u;
 }
 
 // ------------------------------------------------------------------------------------
@@ -525,21 +535,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   } else if (warp >= C::kDrainWarp0) {
     // ---------------------------------------------------------------- dQ drain
     const int qd = warp & 3;
-    // TMEM lane = query row (d = 64, dQ) or head dim (d = 128, dQᵀ); either way 64 columns
-    // and 16 vector adds of 4 values, 512 floats apart in the accumulator.
+    // TMEM lane = query row (d = 64, dQ) or head dim (d = 128, dQᵀ); either way 64 columns.
     const int r = qd * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
-    auto acc_base = [&](int i) {
-      return p.dq_acc + ((D == 64) ? dq_acc_offset(bh, i, p.n_qt, 0, r, D)
-                                   : dq_acc_offset_t(bh, i, p.n_qt, 0, r));
-    };
     int t = 0;
     bool ok = true;
+    // 16 TMEM columns at a time through this warp's two 2 KB staging buffers, each handed to
+    // the TMA engine as one bulk reduce-add (the warp's 32 lanes × 16 columns are contiguous
+    // in the accumulator: 32 query rows × 16 dims at d = 64, 32 dims × 16 query rows at
+    // d = 128); before a buffer is rewritten, the reduction issued from it two chunks
+    // earlier must have read it.
+    const uint32_t stage0 = sbase + C::kDQStage + qd * 2 * C::kDQChunk;
+    int nchunk = 0;
     for (; t < n; ++t) {
       if (!(ok = mbar_wait_warp_inl(&bars->dq_full, t & 1, wc))) break;
       FA_TRACE(20, t);
       tc_fence_after_sync();
-      float* dst = acc_base(i0 + t);
       // 32 columns at a time; the buffer is released once the last columns are in registers.
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -553,21 +564,46 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           if (lane == 0) mbar_arrive(&bars->dq_free);
           FA_TRACE(21, t);
         }
+        {
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4)
-          red_add_v4(dst + (size_t)(h * 8 + c4) * 512, __uint_as_float(x[4 * c4]),
-                     __uint_as_float(x[4 * c4 + 1]), __uint_as_float(x[4 * c4 + 2]),
-                     __uint_as_float(x[4 * c4 + 3]));
+          for (int k2 = 0; k2 < 2; ++k2, ++nchunk) {
+            const uint32_t buf = stage0 + (nchunk & 1) * C::kDQChunk;
+            if (nchunk >= 2) {
+              if (lane == 0) bulk_wait_group_read1();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              st_shared_v4(buf + (c * 32 + lane) * 16, x[16 * k2 + 4 * c], x[16 * k2 + 4 * c + 1],
+                           x[16 * k2 + 4 * c + 2], x[16 * k2 + 4 * c + 3]);
+            fence_proxy_async_smem();  // the staged values, visible to the TMA engine
+            __syncwarp();
+            if (lane == 0) {
+              // TMEM columns 32h + 16k2 …: column group 8h + 4k2 of lanes 32·qd …
+              const int cg = 8 * h + 4 * k2;
+              bulk_reduce_add_f32(p.dq_acc + ((D == 64) ? dq_acc_offset(bh, i0 + t, p.n_qt, cg, qd * 32, D)
+                                                        : dq_acc_offset_t(bh, i0 + t, p.n_qt, cg, qd * 32)),
+                                  buf, C::kDQChunk);
+              bulk_commit_group();
+            }
+          }
+        }
       }
     }
     if (!ok) {
       // Abandoned tiles: poison their dQ rows so that the failure cannot go unseen.
       const float nan = __int_as_float(0x7fc00000);
       for (; t < n; ++t) {
-        float* dst = acc_base(i0 + t);
-        for (int c4 = 0; c4 < 16; ++c4) red_add_v4(dst + (size_t)c4 * 512, nan, nan, nan, nan);
+        for (int c4 = 0; c4 < 16; ++c4) {
+          float* dst = p.dq_acc + ((D == 64) ? dq_acc_offset(bh, i0 + t, p.n_qt, c4, r, D)
+                                             : dq_acc_offset_t(bh, i0 + t, p.n_qt, c4, r));
+          red_add_v4(dst, nan, nan, nan, nan);
+        }
       }
     }
+    // The bulk reductions must be complete (and their sources read) before the CTA exits.
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
     teardown();
   } else {
     // ---------------------------------------------------------------- compute (warps 0-7)

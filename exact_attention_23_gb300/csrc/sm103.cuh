@@ -235,6 +235,18 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
 __device__ __forceinline__ void bulk_wait_group0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// All but this thread's most recent bulk group have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+// gdst[0 .. bytes/4) += the fp32 values at shared address ssrc, as one bulk asynchronous
+// reduction by the TMA engine (both 16-byte aligned, bytes a multiple of 16; tracked by the
+// bulk groups of the issuing thread).
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
+               "r"(ssrc), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
                                           uint64_t* bar) {
   asm volatile(
