@@ -16,7 +16,7 @@ using namespace fa::host;
 
 extern "C" {
 
-// Workspace: [BH][T_pad] fp32 lse2, [BH][T_pad] fp32 D, [BH][T_pad][d] fp32 dQ accumulator,
+// Workspace: [BH][T_pad] fp32 −log2e·LSE, [BH][T_pad] fp32 D, [BH][T_pad][d] fp32 dQ accumulator,
 // each section starting on a 256-byte boundary. Returns 0 for unsupported sizes.
 size_t fa_bwd_workspace_size(int B, int H, int T, int d) {
   if (B <= 0 || H <= 0 || T <= 0 || (d != 64 && d != 128)) return 0;

@@ -86,7 +86,7 @@ struct BwdCfg {
   static constexpr int kStageBytes = 2 * kQTile;
   static constexpr int kDS = kStage0 + kStages * kStageBytes;  // dSᵀ: 2 buffers
   static constexpr int kDSBytes = 128 * kBQ * 2;      // [128 keys][kBQ queries] bf16, 64-col boxes
-  static constexpr int kVecBytes = 2 * kBQ * 4;       // per stage: lse2[kBQ] then D[kBQ]
+  static constexpr int kVecBytes = 2 * kBQ * 4;       // per stage: −lse2[kBQ] then D[kBQ]
   static constexpr int kVec = kDS + 2 * kDSBytes;
   // Each dQ drain warp stages 16 of its TMEM columns for its 32 lanes (2 KB) for a bulk
   // reduce-add, two buffers per warp.
@@ -127,7 +127,7 @@ static_assert(sizeof(BwdBars) <= 256, "barrier block");
 struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  const float* lse2;   // [BH][T_pad] log2(e)·LSE, +∞ on padding rows
+  const float* lse2;   // [BH][T_pad] −log2(e)·LSE, −∞ on padding rows
   const float* dvec;   // [BH][T_pad] D_i, 0 on padding rows
   float* dq_acc;       // fp32 dQ accumulator (unscaled), layout of dq_acc_offset
   int* status;
@@ -181,7 +181,8 @@ __host__ __device__ __forceinline__ size_t dq_acc_offset_t(int bh, int i, int n_
 }
 
 // ------------------------------------------------------------------------------------
-// Preprocessing: D_i = Σ_c dO_ic·O_ic, lse2_i = log2(e)·LSE_i; zero the dQ accumulator.
+// Preprocessing: D_i = Σ_c dO_ic·O_ic, lse2_i = −log2(e)·LSE_i (negated: the main kernel adds
+// it in a packed fp32x2 FMA); zero the dQ accumulator.
 // D/8 consecutive lanes share a row, each reading 8 columns (16 bytes) of O and dO.
 // ------------------------------------------------------------------------------------
 template <int D>
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
     for (int w = L / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
     if (c == 0) {
       dvec[row] = (t < T) ? acc : 0.f;
-      lse2[row] = (t < T) ? lse[(size_t)bh * T + t] * 1.4426950408889634f : __int_as_float(0x7f800000);
+      lse2[row] = (t < T) ? lse[(size_t)bh * T + t] * -1.4426950408889634f : __int_as_float(0xff800000);
     }
   }
   float4* acc4 = reinterpret_cast<float4*>(dq_acc);
@@ -627,16 +628,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->s_free);
-      // Pᵀ = exp2(S·scale·log2e − lse2_q), zero where the key comes after the query
+      // Pᵀ = exp2(S·scale·log2e − log2e·LSE_q), zero where the key comes after the query
+      // (the argument on fp32 pairs; the workspace holds −log2e·LSE)
       float pr[NC];
       const float4* l4 = reinterpret_cast<const float4*>(vec + g * NC);
+      const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
       for (int c = 0; c < NC; c += 4) {
         const float4 l = l4[c / 4];
-        pr[c] = ex2_approx(fmaf(__uint_as_float(s[c]), p.scale_log2, -l.x));
-        pr[c + 1] = ex2_approx(fmaf(__uint_as_float(s[c + 1]), p.scale_log2, -l.y));
-        pr[c + 2] = ex2_approx(fmaf(__uint_as_float(s[c + 2]), p.scale_log2, -l.z));
-        pr[c + 3] = ex2_approx(fmaf(__uint_as_float(s[c + 3]), p.scale_log2, -l.w));
+        float x0, x1, x2, x3;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), c2,
+                         f2_pack(l.x, l.y)), x0, x1);
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c + 2]), __uint_as_float(s[c + 3])), c2,
+                         f2_pack(l.z, l.w)), x2, x3);
+        pr[c] = ex2_approx(x0);
+        pr[c + 1] = ex2_approx(x1);
+        pr[c + 2] = ex2_approx(x2);
+        pr[c + 3] = ex2_approx(x3);
       }
       if (CAUSAL && j * 128 + 127 > i * C::kBQ) {  // a tile the diagonal crosses
         const int rel = j * 128 + r - (i * C::kBQ + g * NC);  // key − first query of the warpgroup
@@ -685,15 +693,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           const float4 da = d4[2 * q4], db = d4[2 * q4 + 1];
           const int c = h * kDPB + q4 * 8;
           const uint32_t* dq8 = dp + q4 * 8;
+          // dS = P ∘ (dP − D) on fp32 pairs
+          const float dd[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
           float ds[8];
-          ds[0] = pr[c] * (__uint_as_float(dq8[0]) - da.x);
-          ds[1] = pr[c + 1] * (__uint_as_float(dq8[1]) - da.y);
-          ds[2] = pr[c + 2] * (__uint_as_float(dq8[2]) - da.z);
-          ds[3] = pr[c + 3] * (__uint_as_float(dq8[3]) - da.w);
-          ds[4] = pr[c + 4] * (__uint_as_float(dq8[4]) - db.x);
-          ds[5] = pr[c + 5] * (__uint_as_float(dq8[5]) - db.y);
-          ds[6] = pr[c + 6] * (__uint_as_float(dq8[6]) - db.z);
-          ds[7] = pr[c + 7] * (__uint_as_float(dq8[7]) - db.w);
+#pragma unroll
+          for (int e = 0; e < 8; e += 2)
+            f2_unpack(f2_mul(f2_pack(pr[c + e], pr[c + e + 1]),
+                             f2_sub(f2_pack(__uint_as_float(dq8[e]), __uint_as_float(dq8[e + 1])),
+                                    f2_pack(dd[e], dd[e + 1]))),
+                      ds[e], ds[e + 1]);
           st_row_chunk_sw128(ds_box, r, ds_chunk0 + c / 8, ds);
         }
       }
