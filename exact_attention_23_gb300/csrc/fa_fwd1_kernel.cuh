@@ -38,8 +38,9 @@
 //   warp  4H        S issuer: S(j) = Q·K(j)ᵀ into S[j mod 2] (one elected thread); TMEM owner
 //   warp  4H + 1    TMA producer (Q per unit; K and V per step through a ring)
 //   warp  4H + 2    P·V issuer: O_h += P_h(j)·V_h(j) from P[j mod 2]
-// With 224 threads (H = 1) every thread may hold 255 registers, with 352 (H = 2) 184: either
-// way the softmax keeps its part of the S row, its P and its state in registers.
+// With 224 threads (H = 1) every thread may hold 255 registers, with 352 (H = 2) 168: either
+// way the softmax keeps its part of the S row, its P and its state in registers without
+// spilling.
 // Tensor memory (512 columns × 128 lanes × 32 bit):
 //   [0,128) S[0]   [128,256) S[1]   [256,256+H·D) O_0 … O_{H−1} (fp32)   then P[0], P[1] (64
 //   columns each: 128 keys as bf16 pairs, half h in columns 32h … of each) — 512 columns.
