@@ -1,7 +1,7 @@
 """GPU parity at the sizes, seeds and launch configuration of bench.py's secondary objects
-(decode, block-sparse, FP8), against the fp64 oracle: every head where the oracle is cheap
-(decode: one query per head), otherwise whole heads picked from the batch (block-sparse)
-or sampled rows (FP8). Tolerances as for the forward: O max-abs ≤ 2e-2, mean-abs ≤ 1e-3,
+(decode, a few new queries, block-sparse, FP8), against the fp64 oracle: every head where the
+oracle is cheap (decode and a few queries: one to 128 query rows per head), otherwise whole
+heads picked from the batch (block-sparse) or sampled rows (FP8). Tolerances as for the forward: O max-abs ≤ 2e-2, mean-abs ≤ 1e-3,
 LSE ≤ 1e-3."""
 
 import numpy as np
@@ -38,6 +38,25 @@ def test_decode_bench_size_every_head():
     # one row per head sees 16384 keys: |O| is small; rounding allowance as for short rows
     _check(o.float().cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, lse_ref,
            "decode B4 H12 Tk16384", 2.0 ** -9 * float(np.abs(o_ref).mean()))
+
+
+@pytest.mark.parametrize("tq", [2, 8, 128])
+def test_few_queries_bench_size_every_head(tq):
+    """B4 H12 d64: the last tq queries of the decode object's T = 16384 draw (seed 20) against
+    all 16384 keys, bottom-right causal, automatic key ranges (bench.py's
+    fwd_kv_few_queries): Tq = 2 on the CUDA-core multi-query kernel, 8 and 128 on the
+    one-tile general form with split ranges."""
+    import torch
+    import exact_attention_23_gb300 as fa
+    B, H, Tk, d = 4, 12, 16384, 64
+    q, k, v = inputs.make_qkv(B, H, Tk, d, seed=20)
+    qm = q[:, :, -tq:].contiguous()
+    o, lse = fa.fwd_kv(qm.cuda(), k.cuda(), v.cuda(), causal=True, n_splits=0)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.attention_general(*(inputs.to_f64_numpy(t) for t in (qm, k, v)),
+                                              True, d ** -0.5)
+    _check(o.float().cpu().double().numpy(), lse.cpu().double().numpy(), o_ref, lse_ref,
+           f"few queries Tq{tq} B4 H12 Tk16384", 2.0 ** -9 * float(np.abs(o_ref).mean()))
 
 
 def test_block_sparse_bench_size_two_heads():
