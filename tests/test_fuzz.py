@@ -120,3 +120,36 @@ def test_fuzz_block_sparse(case):
     o_ref, lse_ref = _ref(q, k, v, d ** -0.5, full)
     _check(o, lse, o_ref, lse_ref,
            f"block-sparse B{B} H{H} T{T} d{d} causal={causal} per_head={per_head} density={density}", v)
+
+
+@pytest.mark.parametrize("case", range(24))
+def test_fuzz_backward(case):
+    """fa_bwd on random shapes against fp32 PyTorch autograd on the GPU, with the
+    scale-relative bounds of the sampled backward checks (max|G − G_ref| ≤ 2e-2·max|G_ref|,
+    mean ≤ 5e-3·mean|G_ref|): the kernel rounds P and dS to bf16 before their products."""
+    import torch
+    import exact_attention_23_gb300 as fa
+    rng = np.random.default_rng(9600 + case)
+    B, H = int(rng.integers(1, 4)), int(rng.integers(1, 9))
+    T = int(rng.choice([int(rng.integers(1, 300)), int(rng.integers(300, 2000))]))
+    d = int(rng.choice([64, 128]))
+    causal = bool(rng.integers(0, 2))
+    scale = float(rng.choice([d ** -0.5, 0.05, -0.1]))
+    q, k, v = (t.cuda() for t in inputs.make_qkv(B, H, T, d, 9700 + case))
+    do = inputs.make_do(B, H, T, d, 9700 + case).cuda()
+    o, lse = fa.fwd(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = fa.bwd(q, k, v, o, lse, do, causal=causal, scale=scale)
+    qf, kf, vf = (t.float().requires_grad_(True) for t in (q, k, v))
+    s = torch.matmul(qf, kf.transpose(-1, -2)) * scale
+    if causal:
+        s = s.masked_fill(~torch.ones(T, T, dtype=torch.bool, device="cuda").tril(), float("-inf"))
+    torch.matmul(torch.softmax(s, dim=-1), vf).backward(do.float())
+    what = f"bwd B{B} H{H} T{T} d{d} causal={causal} scale={scale}"
+    for name, g, r in (("dQ", dq, qf.grad), ("dK", dk, kf.grad), ("dV", dv, vf.grad)):
+        g, r = g.float(), r.float()
+        assert bool(torch.isfinite(g).all()), f"{what}: {name} not finite"
+        err = (g - r).abs()
+        assert err.max().item() <= 2e-2 * r.abs().max().item() + 1e-6, \
+            f"{what}: {name} max-abs {err.max().item():.3e} (max|ref| {r.abs().max().item():.3e})"
+        assert err.mean().item() <= 5e-3 * r.abs().mean().item() + 1e-6, \
+            f"{what}: {name} mean-abs {err.mean().item():.3e} (mean|ref| {r.abs().mean().item():.3e})"
