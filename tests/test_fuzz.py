@@ -2,7 +2,8 @@
 the GPU (softmax(scale·QKᵀ + mask)·V and its logsumexp), over shapes the named workloads do
 not reach: random batch and head counts, ragged lengths on both sides of the short-grid
 switch, both head dims, causal or not, scales of either sign, and for the general forms
-random query/key lengths, key-range counts and block masks. Tolerances: O mean-abs ≤ 1e-3 +
+random query/key lengths, key-range counts and block masks; the FP8 forward against the
+values its e4m3 codes stand for, and the forward on CTA pairs. Tolerances: O mean-abs ≤ 1e-3 +
 2⁻⁹·mean|O_ref| and LSE ≤ 1e-3 on rows that see a key, as for the oracle tests; O max-abs ≤
 max(2e-2, 2⁻⁸·max|V| + 2⁻⁹·max|O_ref| + 1e-3). The kernels round each probability to bf16
 (relative error ≤ 2⁻⁸) before P·V, which moves O_i by at most 2⁻⁸·Σ_j p_ij·|v_j| / l_i ≤
@@ -153,3 +154,40 @@ def test_fuzz_backward(case):
             f"{what}: {name} max-abs {err.max().item():.3e} (max|ref| {r.abs().max().item():.3e})"
         assert err.mean().item() <= 5e-3 * r.abs().mean().item() + 1e-6, \
             f"{what}: {name} mean-abs {err.mean().item():.3e} (mean|ref| {r.abs().mean().item():.3e})"
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_fuzz_fp8(case):
+    """fa_fwd_fp8 (e4m3 query/key codes with per-tensor scales, bf16 V) against fp32 math on
+    the values the codes stand for."""
+    import torch
+    import exact_attention_23_gb300 as fa
+    rng = np.random.default_rng(9800 + case)
+    B, H = int(rng.integers(1, 4)), int(rng.integers(1, 13))
+    T = int(rng.choice([int(rng.integers(1, 400)), int(rng.integers(400, 3000))]))
+    d = int(rng.choice([64, 128]))
+    causal = bool(rng.integers(0, 2))
+    q8, sq, k8, sk, v = inputs.make_qk_fp8(B, H, T, d, 9900 + case)
+    o, lse = fa.fwd_fp8(q8.cuda(), sq, k8.cuda(), sk, v.cuda(), causal=causal)
+    qf = q8.cuda().view(torch.float8_e4m3fn).float() * sq
+    kf = k8.cuda().view(torch.float8_e4m3fn).float() * sk
+    mask = torch.ones(T, T, dtype=torch.bool, device="cuda").tril() if causal else None
+    o_ref, lse_ref = _ref(qf, kf, v.cuda(), d ** -0.5, mask)
+    _check(o, lse, o_ref, lse_ref, f"fp8 B{B} H{H} T{T} d{d} causal={causal}", v)
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_fuzz_cta_pair(case):
+    """The forward on CTA pairs (FA_FLAG_CTA_PAIR, head dim 64) on random shapes."""
+    import torch
+    import exact_attention_23_gb300 as fa
+    rng = np.random.default_rng(10000 + case)
+    B, H = int(rng.integers(1, 5)), int(rng.integers(1, 17))
+    T = int(rng.choice([int(rng.integers(1, 600)), int(rng.integers(600, 4000))]))
+    causal = bool(rng.integers(0, 2))
+    scale = float(rng.choice([0.125, -0.1]))
+    q, k, v = (t.cuda() for t in inputs.make_qkv(B, H, T, 64, 10100 + case))
+    o, lse = fa.fwd(q, k, v, causal=causal, scale=scale, flags=fa.FA_FLAG_CTA_PAIR)
+    mask = torch.ones(T, T, dtype=torch.bool, device="cuda").tril() if causal else None
+    o_ref, lse_ref = _ref(q, k, v, scale, mask)
+    _check(o, lse, o_ref, lse_ref, f"pair B{B} H{H} T{T} causal={causal} scale={scale}", v)
