@@ -370,6 +370,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   const WaitCtl wc{&bars->abort, p.status, p.timeout_ns};
   const WaitCtl drain = drain_ctl(p.timeout_ns);
+  // Bounded warp waits. At d = 64 (bf16) lane 0 alone polls: a waiting control warp then
+  // takes fewer issue slots from the softmax warps on its sub-partition (0.9 % faster); the
+  // e4m3 kernel, whose waits sit closer to its critical path, keeps every lane polling.
+  auto wait_w = [](uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+    if constexpr (D == 64 && !QK8) return mbar_wait_warp_lp(bar, parity, w);
+    else return mbar_wait_warp(bar, parity, w);
+  };
 
   if (warp == 9) {
     // ------------------------------------------------------------ TMA producer
@@ -394,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit u = unit_of<CAUSAL, GEN>(p, L);
       const int qb = qn % C::kQBufs;
       if (qn >= C::kQBufs &&
-          !mbar_wait_warp(&bars->q_empty[qb], ((qn / C::kQBufs) - 1) & 1, wc)) { ok = false; break; }
+          !wait_w(&bars->q_empty[qb], ((qn / C::kQBufs) - 1) & 1, wc)) { ok = false; break; }
       const bool load = load_q && (later_q || qn == 0);
       if (load) ++ql;
       if (load && leader) {
@@ -419,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int st = g % C::kStages;
         const int use = g / C::kStages;
-        if (use > 0 && !mbar_wait_warp(&bars->kv_empty[st], (use - 1) & 1, wc)) { ok = false; break; }
+        if (use > 0 && !wait_w(&bars->kv_empty[st], (use - 1) & 1, wc)) { ok = false; break; }
         FA_TRACE(1, j);
         if (leader) {
           mbar_arrive_expect_tx(&bars->k_full[st], C::kQKTileBytes);
@@ -440,12 +447,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (Q was loaded for the CTA's first ql units; buffer b served every kQBufs-th of them.)
     for (int b = 0; b < C::kQBufs && b < ql; ++b) {
       const int last = (ql - 1 - b) / C::kQBufs;  // last loaded use of buffer b
-      mbar_wait_warp(&bars->q_full[b], last & 1, drain);
+      wait_w(&bars->q_full[b], last & 1, drain);
     }
     for (int st = 0; st < C::kStages && st < g; ++st) {
       const int last_use = (g - 1 - st) / C::kStages;
-      mbar_wait_warp(&bars->k_full[st], last_use & 1, drain);
-      mbar_wait_warp(&bars->v_full[st], last_use & 1, drain);
+      wait_w(&bars->k_full[st], last_use & 1, drain);
+      wait_w(&bars->v_full[st], last_use & 1, drain);
     }
   } else if (warp == 8 || warp == 10) {
     // ------------------------------------------------------------ MMA issuers
@@ -496,13 +503,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (L >= p.total_units) continue;
         const Unit u = unit_of<CAUSAL, GEN>(p, L);
         const int qb = qn % C::kQBufs;
-        if (!mbar_wait_warp(&bars->q_full[qb], (qn / C::kQBufs) & 1, wc)) { ok = false; break; }
+        if (!wait_w(&bars->q_full[qb], (qn / C::kQBufs) & 1, wc)) { ok = false; break; }
         UnitSteps<CAUSAL, GEN> us;
         if constexpr (GEN) us.begin(p, u);
         for (int j = 0; j < u.n_steps; ++j, ++g) {
           if constexpr (GEN) us.next(u, j);
           const int st = g % C::kStages;
-          if (!mbar_wait_warp(&bars->k_full[st], (g / C::kStages) & 1, wc)) { ok = false; break; }
+          if (!wait_w(&bars->k_full[st], (g / C::kStages) & 1, wc)) { ok = false; break; }
           tc_fence_after_sync();
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
@@ -511,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // S_i may be overwritten once its softmax has read it (P in its own columns)
               // or, when P_i lives in S_i's columns, once P_i·V has consumed P_i.
               uint64_t* freed = C::kSepP ? &bars->s_free[i] : &bars->pv_done[i];
-              if (!mbar_wait_warp(freed, (ns[i] - 1) & 1, wc)) { ok = false; break; }
+              if (!wait_w(freed, (ns[i] - 1) & 1, wc)) { ok = false; break; }
               tc_fence_after_sync();
             }
             issue_s(qb, i, st);
@@ -562,18 +569,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < u.n_steps; ++j, ++g) {
           if constexpr (GEN) us.next(u, j);
           const int st = g % C::kStages;
-          if (!mbar_wait_warp(&bars->v_full[st], (g / C::kStages) & 1, wc)) { ok = false; break; }
+          if (!wait_w(&bars->v_full[st], (g / C::kStages) & 1, wc)) { ok = false; break; }
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             if (GEN ? !us.act[i] : j >= u.nkv[i]) continue;
             if (jt[i] == 0 && nunits[i] > 0) {
               // This unit's first P·V overwrites O_i: the previous unit's O_i must have
               // been read out.
-              if (!mbar_wait_warp(&bars->o_free[i], (nunits[i] - 1) & 1, wc)) { ok = false; break; }
+              if (!wait_w(&bars->o_free[i], (nunits[i] - 1) & 1, wc)) { ok = false; break; }
             }
 #pragma unroll
             for (int h = 0; h < C::kPParts; ++h) {
-              if (!mbar_wait_warp(&bars->p_full[i][h], np[i] & 1, wc)) { ok = false; break; }
+              if (!wait_w(&bars->p_full[i][h], np[i] & 1, wc)) { ok = false; break; }
               if (h == 0) FA_TRACE(11 + i, j);
               tc_fence_after_sync();
               issue_pv(i, st, jt[i] > 0, h);
@@ -593,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Nothing may still be running on the tensor core when TMEM is released.
     commit(&bars->mma_done);
-    mbar_wait_warp(&bars->mma_done, 0, drain);
+    wait_w(&bars->mma_done, 0, drain);
   } else {
     // ------------------------------------------------------------ softmax warpgroups
     const int wg = warp >> 2;
@@ -738,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Finishes the pending unit once its last P·V is done (already waited for when
     // `waited`).
     auto flush_pending = [&](bool waited) {
-      const bool good = waited || (ok && mbar_wait_warp(&bars->pv_done[wg], (gs - 1) & 1, wc));
+      const bool good = waited || (ok && wait_w(&bars->pv_done[wg], (gs - 1) & 1, wc));
       if (good) {
         if (!waited) tc_fence_after_sync();
         uint32_t o[D];
@@ -798,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           ++kt;
         }
-        if (!mbar_wait_warp(&bars->s_full[wg], gs & 1, wc)) { ok = false; break; }
+        if (!wait_w(&bars->s_full[wg], gs & 1, wc)) { ok = false; break; }
         FA_TRACE(30 + wg, j);
         tc_fence_after_sync();
         const int k0 = kt * kBlockN;
@@ -927,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // must be stable: the previous P·V done. 16 columns at a time (the second half
             // of S may still be live).
             if (C::kSepP && gs > 0) {
-              if (!mbar_wait_warp(&bars->pv_done[wg], (gs - 1) & 1, wc)) { ok = false; break; }
+              if (!wait_w(&bars->pv_done[wg], (gs - 1) & 1, wc)) { ok = false; break; }
               tc_fence_after_sync();
               waited = true;
             }
@@ -945,7 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (C::kSepP) {
             // These P_i columns are free once the matching part of the previous P_i·V is done.
             if (gs > 0 && !waited) {
-              if (!mbar_wait_warp(h == C::kPParts - 1 ? &bars->pv_done[wg] : &bars->pv_part[wg][h],
+              if (!wait_w(h == C::kPParts - 1 ? &bars->pv_done[wg] : &bars->pv_part[wg][h],
                                   (gs - 1) & 1, wc)) { ok = false; break; }
               tc_fence_after_sync();
             }
@@ -985,7 +992,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // Epilogue at once (D = 128, and the partial rows): O / l and the logsumexp, once this
       // unit's last P·V is done.
-      const bool good = mbar_wait_warp(&bars->pv_done[wg], (gs - 1) & 1, wc);
+      const bool good = wait_w(&bars->pv_done[wg], (gs - 1) & 1, wc);
       FA_TRACE(24 + wg, 0);
       if (good) {
         tc_fence_after_sync();
