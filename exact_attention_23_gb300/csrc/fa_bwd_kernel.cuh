@@ -22,15 +22,18 @@
 //   fa_bwd_dq_kernel     accumulator × scale → bf16 dQ.
 //
 // Main kernel: kCWG compute warpgroups (4 at d = 64: 23 warps, 736 threads; 2 at d = 128:
-// 15 warps, 480 threads), then:
+// 16 warps, 512 threads), then:
 //   warps 0 .. 4·kCWG−1   compute: warpgroup g owns query columns 32·g .. 32·g+31 of each
 //                         tile (thread = key row); no exchange between warpgroups is needed,
 //                         since P comes from the saved LSE, column by column
 //   next 4 warps          dQ drain: TMEM → registers → shared memory → bulk reduce-adds
 //                         into the fp32 accumulator by the TMA engine
 //   next warp             score issuer: Sᵀ and dPᵀ MMAs (one elected thread); TMEM owner
-//   next warp             gradient issuer: dV, dK and dQ MMAs (one elected thread)
-//   last warp             TMA producer
+//   next warp             gradient issuer: dV, dK and dQ MMAs (one elected thread); at
+//                         d = 128 dV and dK only
+//   next warp             TMA producer
+//   last warp (d = 128)   dQ issuer: the dQᵀ MMAs, from the fourth sub-partition (measured
+//                         4 % faster there; at d = 64 a separate dQ issuer was 2 % slower)
 // (More compute warps hide more of the latency of each tile's chain of TMEM loads and
 // stores; at d = 64 four warpgroups of 32 columns measured 4 % faster than two of 64.)
 // Two issuers, because MMAs into different accumulators are not ordered with one another
@@ -74,7 +77,9 @@ struct BwdCfg {
   static constexpr int kScoreWarp = kDrainWarp0 + 4;
   static constexpr int kGradWarp = kScoreWarp + 1;
   static constexpr int kLoadWarp = kScoreWarp + 2;
-  static constexpr int kThreads = (kLoadWarp + 1) * 32;
+  static constexpr bool kSplitQ = (D == 128);  // dQ products issued by a warp of their own
+  static constexpr int kGradQWarp = kScoreWarp + 3;
+  static constexpr int kThreads = (kSplitQ ? kGradQWarp + 1 : kLoadWarp + 1) * 32;
   static constexpr int kBox = 128 * 64 * 2;           // 128 rows × 64 bf16 columns = 16 KB
   static constexpr int kQBox = kBQ * 64 * 2;          // kBQ rows × 64 columns
   static constexpr int kKVTile = 128 * D * 2;         // a K or V tile
@@ -342,7 +347,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bars->ds_full[s], C::kComputeWarps);
-      mbar_init(&bars->ds_free[s], 1);
+      mbar_init(&bars->ds_free[s], C::kSplitQ ? 2 : 1);  // after dK (and dQ, if split)
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, C::kComputeWarps);
@@ -353,7 +358,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, 4);
     mbar_init(&bars->score_done, 1);
-    mbar_init(&bars->grad_done, 1);
+    mbar_init(&bars->grad_done, C::kSplitQ ? 2 : 1);
     bars->abort = 0u;
     fence_mbar_init();
   }
@@ -507,7 +512,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const int b = t & 1;
       const uint32_t ds_s = sbase + C::kDS + b * C::kDSBytes;
       if (!(ok = mbar_wait_warp_inl(&bars->ds_full[b], (t >> 1) & 1, wc))) break;
-      if (t > 0 && !(ok = mbar_wait_warp_inl(&bars->dq_free, (t - 1) & 1, wc))) break;
+      if (!C::kSplitQ && t > 0 && !(ok = mbar_wait_warp_inl(&bars->dq_free, (t - 1) & 1, wc))) break;
       FA_TRACE(4, t);
       tc_fence_after_sync();
       if (lane == 0) {
@@ -515,6 +520,35 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int kk = 0; kk < C::kBQ / 16; ++kk)
           mma_ss(tmem + C::kColDK, kmaj(ds_s, kk, C::kBox), mnmaj(q_s(st), kk, C::kQBox), kIdK,
                  (t > 0 || kk > 0));
+#pragma unroll
+        for (int kk = 0; kk < (C::kSplitQ ? 0 : 8); ++kk) {  // K = 128 keys
+          if constexpr (D == 64)
+            mma_ss(tmem + C::kColDQ, mnmaj(ds_s, kk, C::kBox), mnmaj(k_s, kk, C::kBox), kIdQ, kk > 0);
+          else
+            mma_ss(tmem + C::kColDQ, mnmaj(k_s, kk, C::kBox), mnmaj(ds_s, kk, C::kBox), kIdQ, kk > 0);
+        }
+        if constexpr (!C::kSplitQ) mma_commit(&bars->dq_full);
+        mma_commit(&bars->ds_free[b]);
+        mma_commit(&bars->q_empty[st]);
+      }
+      __syncwarp();
+      if (++st == NS) st = 0;
+    }
+    if (lane == 0) mma_commit(&bars->grad_done);
+    __syncwarp();
+  } else if (C::kSplitQ && warp == C::kGradQWarp) {
+    // ---------------------------------------------------------------- dQ issuer (d = 128)
+    // dQ_iᵀ = K_jᵀ·dSᵀ once this tile's dSᵀ is stored and the previous dQ has been drained.
+    constexpr uint32_t kIdQ = idesc_bf16_ab(128, (D == 64) ? D : C::kBQ, true, true);
+    const uint32_t k_s = sbase + C::kK;
+    bool ok = true;
+    for (int t = 0; t < n && ok; ++t) {
+      const int b = t & 1;
+      const uint32_t ds_s = sbase + C::kDS + b * C::kDSBytes;
+      if (!(ok = mbar_wait_warp_inl(&bars->ds_full[b], (t >> 1) & 1, wc))) break;
+      if (t > 0 && !(ok = mbar_wait_warp_inl(&bars->dq_free, (t - 1) & 1, wc))) break;
+      tc_fence_after_sync();
+      if (lane == 0) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {  // K = 128 keys
           if constexpr (D == 64)
@@ -524,10 +558,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
         mma_commit(&bars->dq_full);
         mma_commit(&bars->ds_free[b]);
-        mma_commit(&bars->q_empty[st]);
       }
       __syncwarp();
-      if (++st == NS) st = 0;
     }
     if (lane == 0) mma_commit(&bars->grad_done);
     __syncwarp();
