@@ -707,8 +707,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (t >= 2 && !(ok = mbar_wait_warp_inl(&bars->ds_free[b], ((t >> 1) - 1) & 1, wc))) break;
       FA_TRACE(15, t);
       tc_fence_after_sync();
-      // dPᵀ for this warpgroup's columns (NC = 64: in two halves, to stay within the
-      // registers of 15 warps)
+      // dPᵀ for this warpgroup's columns (were a warpgroup to own NC = 64 columns: in two
+      // halves, to stay within the register budget)
       constexpr int kDPB = (NC > 32) ? 32 : NC;  // columns per dPᵀ block
 #pragma unroll
       for (int h = 0; h < NC / kDPB; ++h) {
