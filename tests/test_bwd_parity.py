@@ -211,12 +211,14 @@ def test_bwd_workspace_reuse_and_determinism():
     assert diff <= 2e-2 * a[0].float().abs().max().item()
 
 
-def test_bwd_timeout_reports_and_poisons():
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_timeout_reports_and_poisons(d):
     """A wait that runs out (the query loads are withheld on purpose) stores
-    FA_ERR_TIMEOUT and leaves NaN gradients; the next normal call is correct."""
+    FA_ERR_TIMEOUT and leaves NaN gradients; the next normal call is correct. Head dim 128
+    has its own warp roles (a separate dQ issuer), so both are run."""
     torch = _torch()
     import exact_attention_23_gb300 as fa
-    w = inputs.WORKLOADS["tiny_causal"]
+    w = inputs.WORKLOADS["tiny_causal"] if d == 64 else inputs.Workload("tiny_wide", 1, 2, 256, 128, True, 12)
     q, k, v = inputs.workload_qkv(w)
     do = inputs.workload_do(w)
     qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
